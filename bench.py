@@ -1,0 +1,409 @@
+"""Benchmark: SSB G build + reconstruction + batched scoring on one GB300.
+
+One step = one pass of the whole hot path over the full-size synthetic scan
+(512^2 scan, 192^2 uint16 detector, ~9.35k bright-field pixels):
+  ssb_build_G      frames -> G(q,k) half plane             (the build)
+  ssb_reconstruct  one aberration set -> O, N, phase image (the recon)
+  ssb_score_batch  8 aberration sets over the 0.2-0.9 1/A band -> scores
+
+Prints one JSON line.  `value` is ms per step (device time, inputs resident
+in HBM, max over ranks); `e2e` is the same step through the public API with
+host buffers (pinned frames copied in, phase and scores copied out, every
+step).  `--impl reference` times the CPU float64 oracle on a bounded sample of
+the same workload instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "ms per SSB recon + G-build HBM GB/s (512^2 scan, 192^2 det, ~9.3k BF px)"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="full", choices=["full", "large", "small", "tiny"])
+    p.add_argument("--sets", type=int, default=8)
+    p.add_argument("--e2e-steps", type=int, default=3)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-sample-bf", type=int, default=0, help="BF pixels in the oracle sample (0: auto)")
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (replicas: every rank runs its own full problem)
+# ----------------------------------------------------------------------------
+
+def dist_setup(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if ws > 1 and args.impl == "ours":
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group(backend="nccl")
+        pg = dist
+    return ws, rank, local, pg
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def allmax(pg, x, device=None):
+    if pg is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                    power.append(float(parts[3]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(nm)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------
+# oracle (CPU float64) timing on a bounded sample
+# ----------------------------------------------------------------------------
+
+def oracle_sample(d, bf_all, band, sets, n_sample, cols_host):
+    """Time the CPU oracle on `n_sample` BF pixels of the workload: G build,
+    one reconstruction's reduction over the whole half plane and the 8-set band
+    reduction, then scale to all BF pixels (every stage is linear in N_bf; the
+    O(n^2 log n) image step is added once)."""
+    from oracle import ssb_oracle as O
+    g, ab = d["geom"], d["ab"]
+    n = g.n
+    rng = np.random.default_rng(0)
+    pick = np.sort(rng.choice(len(bf_all), size=n_sample, replace=False))
+    bf = bf_all[pick]
+    frames_sub = cols_host[:, pick].reshape(n, n, 1, n_sample)  # fake (n, n, 1, s) layout
+    idx = np.arange(n_sample, dtype=np.int32)
+    t0 = time.perf_counter()
+    G = O.build_G(frames_sub, idx)
+    t1 = time.perf_counter()
+    Oq, Nq = O.reduce(G, g, ab, bf)
+    t2 = time.perf_counter()
+    O.phase_image(Oq, Nq, O.g0_mean(G), n)
+    t3 = time.perf_counter()
+    for s in sets:
+        O.reduce(G, g, s, bf, entries=band)
+    t4 = time.perf_counter()
+    scale = len(bf_all) / n_sample
+    per_step = (t1 - t0) * scale + (t2 - t1) * scale + (t3 - t2) + (t4 - t3) * scale
+    return {"ms_per_step": per_step * 1e3, "sample_seconds": t4 - t0,
+            "build_ms": (t1 - t0) * scale * 1e3, "recon_ms": ((t2 - t1) * scale + (t3 - t2)) * 1e3,
+            "score_ms": (t4 - t3) * scale * 1e3, "n_sample": n_sample}
+
+
+def cpu_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+# ----------------------------------------------------------------------------
+# reference arm: the CPU oracle as it stands
+# ----------------------------------------------------------------------------
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return 0
+    from synth import configs as C
+    from synth import forward as F
+    import torch
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    d = F.make_torch_dataset(args.workload, device=dev) if args.workload in ("full", "large") \
+        else F.make_numpy_dataset(args.workload)
+    g, ab = d["geom"], d["ab"]
+    from oracle import ssb_oracle as O
+    bf = O.bf_indices(g, ab.tilt_x_rad, ab.tilt_y_rad)
+    band = O.band_indices(g, *C.BAND_INVA)
+    sets = C.perturbed_sets(ab, args.sets, seed=4)
+    n = g.n
+    if torch.is_tensor(d["frames"]):
+        cols = d["frames"].view(n * n, -1).index_select(1, torch.from_numpy(bf).to(d["frames"].device).long())
+        cols = cols.cpu().numpy().view(np.uint16)
+    else:
+        cols = d["frames"].reshape(n * n, -1)[:, bf]
+    n_sample = args.cpu_sample_bf or max(1, min(len(bf), 16 if n >= 512 else 64))
+    times = []
+    info = None
+    for i in range(args.warmup + args.steps):
+        info = oracle_sample(d, bf, band, sets, n_sample, cols)
+        if i >= args.warmup:
+            times.append(info["ms_per_step"])
+    v = statistics.mean(times)
+    line = {"metric": METRIC, "value": v, "unit": "ms", "impl": "reference", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": v, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{args.workload}: {n}^2 scan, {g.det_y}^2 uint16 detector, "
+                                   f"{len(bf)} BF px; step = G build + 1 reconstruction + "
+                                   f"{args.sets}-set band scoring",
+                       "sample": f"{n_sample} of {len(bf)} BF pixels per step, scaled by N_bf"},
+            "cpu_baseline": {"value": v, "unit": "ms", "cores": 1, "kind": "oracle",
+                             "sample": f"{n_sample} BF pixels per step (all q), linear scaling to {len(bf)}"},
+            "e2e": {"value": v, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+
+def run_ours(args, ws, rank, local, pg):
+    import torch
+    import electron_microscopy_gb300 as ssb
+    from synth import configs as C
+    from synth import forward as F
+
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ssb.load()
+
+    d = F.make_torch_dataset(args.workload, device=dev) if args.workload in ("full", "large") \
+        else None
+    if d is None:
+        dn = F.make_numpy_dataset(args.workload)
+        fr = dn["frames"]
+        fr_t = torch.from_numpy(fr.view(np.int16) if fr.dtype == np.uint16 else fr).to(dev)
+        d = {**dn, "frames": fr_t, "max_count": int(fr.max())}
+    frames = d["frames"]
+    geom, ab = d["geom"], d["ab"]
+    n, h = geom.n, geom.n // 2 + 1
+    bf = ssb.bf_indices(geom, ab)
+    n_bf = len(bf)
+    bfd = torch.from_numpy(bf).to(dev)
+    band = ssb.band_indices(geom, *C.BAND_INVA)
+    band_d = torch.from_numpy(band).to(dev)
+    nq = len(band)
+    sets = C.perturbed_sets(ab, args.sets, seed=4)
+    B = len(sets)
+
+    G = torch.empty((n_bf, n, h), dtype=torch.complex64, device=dev)
+    Od = torch.empty((n, h), dtype=torch.complex64, device=dev)
+    Nd = torch.empty((n, h), dtype=torch.int32, device=dev)
+    ph = torch.empty((n, n), dtype=torch.float32, device=dev)
+    Ob = torch.empty((B, nq), dtype=torch.complex64, device=dev)
+    Nb = torch.empty((B, nq), dtype=torch.int32, device=dev)
+    sc = torch.empty((B,), dtype=torch.float64, device=dev)
+    ws_b = ssb.Workspace(ssb.workspace_bytes(geom, n_bf, ssb.OP_BUILD), dev)
+    ws_r = ssb.Workspace(ssb.workspace_bytes(geom, n_bf, ssb.OP_RECON), dev)
+    ws_s = ssb.Workspace(ssb.workspace_bytes(geom, n_bf, ssb.OP_SCORE, B, nq), dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(fr=None):
+        ssb.build_G(frames if fr is None else fr, geom, bfd, G=G, ws=ws_b, stream=stream)
+        ssb.reconstruct(G, geom, bfd, ab, O=Od, N=Nd, phase=ph, ws=ws_r, stream=stream)
+        ssb.score_batch(G, geom, bfd, sets, band_d, O=Ob, N=Nb, score=sc, ws=ws_s, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+
+    # timed region (device time on the launching stream)
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    clocks = ClockSampler(vis.split(",")[local] if vis else str(local))
+    clocks.start()
+    time.sleep(0.3)
+    barrier(pg)
+    torch.cuda.synchronize()
+    l0 = ssb.launch_count()
+    t_wall0 = time.perf_counter()
+    for i in range(K):
+        e0, e1, e2, e3 = ev[i]
+        e0.record(stream)
+        ssb.build_G(frames, geom, bfd, G=G, ws=ws_b, stream=stream)
+        e1.record(stream)
+        ssb.reconstruct(G, geom, bfd, ab, O=Od, N=Nd, phase=ph, ws=ws_r, stream=stream)
+        e2.record(stream)
+        ssb.score_batch(G, geom, bfd, sets, band_d, O=Ob, N=Nb, score=sc, ws=ws_s, stream=stream)
+        e3.record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    launches = ssb.launch_count() - l0
+    barrier(pg)
+    clk = clocks.stop()
+    b_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    r_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    s_ms = [ev[i][2].elapsed_time(ev[i][3]) for i in range(K)]
+    tot = ev[0][0].elapsed_time(ev[K - 1][3])
+    ms_step = allmax(pg, tot / K, dev)
+
+    # algorithmic work
+    bytes_build = n_bf * n * n * (2 if frames.element_size() == 2 else 4) + n_bf * n * h * 8
+    bytes_recon = n_bf * n * h * 8
+    bytes_score = n_bf * nq * 8
+    terms = int(Nb.sum().item())
+    build_ms = statistics.mean(b_ms)
+    recon_ms = statistics.mean(r_ms)
+    score_ms = statistics.mean(s_ms)
+    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(peaks_path):
+        peaks = json.load(open(peaks_path))
+        hbm = float(peaks["hbm_gbs"])
+        peak_src = "measured"
+    else:
+        hbm = 6800.0
+        peak_src = "fallback"
+    achieved = bytes_build / (build_ms * 1e-3) / 1e9
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        host = torch.empty(frames.shape, dtype=frames.dtype, pin_memory=True)
+        host.copy_(frames)
+        ph_h = torch.empty(ph.shape, dtype=ph.dtype, pin_memory=True)
+        sc_h = torch.empty(sc.shape, dtype=sc.dtype, pin_memory=True)
+        fr2 = torch.empty_like(frames)
+        E = max(1, args.e2e_steps)
+        torch.cuda.synchronize()
+        barrier(pg)
+        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ea.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(E):
+                fr2.copy_(host, non_blocking=True)
+                step(fr2)
+                ph_h.copy_(ph, non_blocking=True)
+                sc_h.copy_(sc, non_blocking=True)
+        eb.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = allmax(pg, ea.elapsed_time(eb) / E, dev)
+        e2e = {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": host.numel() * host.element_size(),
+               "d2h_bytes_per_step": ph_h.numel() * 4 + sc_h.numel() * 8, "steps": E}
+        del host, fr2
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cols = frames.view(n * n, -1).index_select(1, bfd.long()).cpu().numpy().view(np.uint16) \
+            if frames.element_size() == 2 else frames.view(n * n, -1).index_select(1, bfd.long()).cpu().numpy()
+        ns = min(n_bf, args.cpu_sample_bf or (48 if n >= 512 else 64))
+        info = oracle_sample({"geom": geom, "ab": ab}, bf, band, sets, ns, cols)
+        cpu = {"value": info["ms_per_step"], "unit": "ms", "cores": 1, "kind": "oracle",
+               "sample": f"{ns} of {n_bf} BF pixels (all q, 1 recon + {B}-set band), scaled linearly by N_bf; "
+                         f"{info['sample_seconds']:.1f} s of CPU work",
+               "build_ms": info["build_ms"], "recon_ms": info["recon_ms"], "score_ms": info["score_ms"]}
+
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": ms_step, "unit": "ms", "n_gpus": ws, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_step, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {n}^2 scan, {geom.det_y}^2 uint16 detector, {n_bf} BF px, "
+                               f"band {nq} q, {B} sets",
+                   "step": "ssb_build_G + ssb_reconstruct + ssb_score_batch(B=8)",
+                   "l2": "inputs larger than L2 (frames %.1f GB, G %.2f GB); no flush" % (
+                       frames.numel() * frames.element_size() / 1e9, n_bf * n * h * 8 / 1e9),
+                   "parallelism": f"replicas x{ws}"},
+        "stages": {"build_ms": build_ms, "build_GBs": achieved, "recon_ms": recon_ms,
+                   "recon_GBs": bytes_recon / (recon_ms * 1e-3) / 1e9,
+                   "score_ms": score_ms, "score_GBs": bytes_score / (score_ms * 1e-3) / 1e9,
+                   "score_terms": terms, "score_terms_per_s": terms / (score_ms * 1e-3),
+                   "max_count": d.get("max_count")},
+        "roofline": {"bound": "hbm", "kernel": "ssb_build_G (row + column passes)", "achieved": achieved,
+                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                     "peak_source": peak_src, "algorithmic_bytes": bytes_build},
+        "clocks": clk, "gpu_launches": launches, "wall_s_timed": t_wall,
+        "e2e": e2e, "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse()
+    ws, rank, local, pg = dist_setup(args)
+    try:
+        if args.impl == "reference":
+            return run_reference(args, ws, rank)
+        return run_ours(args, ws, rank, local, pg)
+    finally:
+        if pg is not None:
+            pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

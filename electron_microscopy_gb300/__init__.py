@@ -1,0 +1,252 @@
+"""GB300 single-sideband (SSB) direct ptychography: Python binding of libssb.
+
+The functions here only marshal arguments (torch tensors -> device pointers,
+dataclasses -> C structs, the current CUDA stream) and call the C ABI declared
+in ``include/ssb.h``; every step of the computation runs in the library's
+CUDA kernels.  There is no fallback: if ``libssb.so`` is missing or a GPU call
+fails, these functions raise.
+
+Typical use::
+
+    import electron_microscopy_gb300 as ssb
+    bf = ssb.bf_indices(geom, base_set)                  # numpy int32 (host)
+    G = ssb.build_G(frames, geom, bf_dev)                # frames: cuda tensor
+    O, N, phase = ssb.reconstruct(G, geom, bf_dev, base_set)
+    O_b, N_b, score = ssb.score_batch(G, geom, bf_dev, sets, band_dev)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libssb.so")
+
+SSB_OK, SSB_INVALID_ARG, SSB_UNSUPPORTED, SSB_WORKSPACE_TOO_SMALL, SSB_CUDA_ERROR = range(5)
+SSB_U16, SSB_F32 = 0, 1
+OP_BUILD, OP_RECON, OP_SCORE = 0, 1, 2
+MAX_SETS = 8
+
+STATUS_NAMES = {0: "SSB_OK", 1: "SSB_INVALID_ARG", 2: "SSB_UNSUPPORTED",
+                3: "SSB_WORKSPACE_TOO_SMALL", 4: "SSB_CUDA_ERROR"}
+
+EXPORTED = ("ssb_bf_indices", "ssb_band_indices", "ssb_workspace_bytes", "ssb_build_G",
+            "ssb_reconstruct", "ssb_score_batch", "ssb_last_error", "ssb_launch_count")
+
+
+class Geometry(ctypes.Structure):
+    _fields_ = [("n", ctypes.c_int), ("det_y", ctypes.c_int), ("det_x", ctypes.c_int),
+                ("scan_step_A", ctypes.c_double), ("det_pitch_invA", ctypes.c_double),
+                ("wavelength_A", ctypes.c_double), ("semiangle_rad", ctypes.c_double),
+                ("det_center_y", ctypes.c_double), ("det_center_x", ctypes.c_double)]
+
+
+ABERR_FIELDS = ("C10", "C12a", "C12b", "C21a", "C21b", "C23a", "C23b", "C30", "C32a", "C32b",
+                "C34a", "C34b", "tilt_x_rad", "tilt_y_rad")
+
+
+class Aberr(ctypes.Structure):
+    _fields_ = [(f, ctypes.c_double) for f in ABERR_FIELDS]
+
+
+class SSBError(RuntimeError):
+    def __init__(self, fn, code, msg):
+        super().__init__(f"{fn} -> {STATUS_NAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+_lib = None
+
+
+def load(path: str | None = None):
+    """Load libssb.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"{p} is missing: build it with __graft_entry__.build() "
+                           "or python -m electron_microscopy_gb300._build")
+    lib = ctypes.CDLL(p)
+    c_int, c_size, c_vp, c_d = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_double
+    G_p, A_p = ctypes.POINTER(Geometry), ctypes.POINTER(Aberr)
+    i32p, ip = ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int)
+    lib.ssb_bf_indices.argtypes = [G_p, A_p, i32p, ip]
+    lib.ssb_band_indices.argtypes = [G_p, c_d, c_d, i32p, ip]
+    lib.ssb_workspace_bytes.argtypes = [G_p, c_int, c_int, c_int, c_int]
+    lib.ssb_workspace_bytes.restype = c_size
+    lib.ssb_build_G.argtypes = [c_vp, c_int, G_p, c_vp, c_int, c_vp, c_vp, c_size, c_vp]
+    lib.ssb_reconstruct.argtypes = [c_vp, G_p, c_vp, c_int, A_p, c_vp, c_vp, c_vp, c_vp, c_size, c_vp]
+    lib.ssb_score_batch.argtypes = [c_vp, G_p, c_vp, c_int, A_p, c_int, c_vp, c_int, c_vp, c_vp, c_vp,
+                                    c_vp, c_size, c_vp]
+    lib.ssb_last_error.restype = ctypes.c_char_p
+    lib.ssb_launch_count.restype = ctypes.c_longlong
+    for fn in ("ssb_bf_indices", "ssb_band_indices", "ssb_build_G", "ssb_reconstruct",
+               "ssb_score_batch"):
+        getattr(lib, fn).restype = c_int
+    _lib = lib
+    return lib
+
+
+def _check(fn, code):
+    if code != SSB_OK:
+        raise SSBError(fn, code, load().ssb_last_error().decode())
+
+
+def to_geometry(g) -> Geometry:
+    if isinstance(g, Geometry):
+        return g
+    return Geometry(*g.astuple())
+
+
+def to_aberr(a) -> Aberr:
+    if isinstance(a, Aberr):
+        return a
+    return Aberr(*a.astuple())
+
+
+def _ptr(t):
+    return ctypes.c_void_p(int(t.data_ptr())) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(stream=None):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(int(s.cuda_stream))
+
+
+# ----------------------------------------------------------------------------
+# host-only entry points
+# ----------------------------------------------------------------------------
+
+def bf_indices(geom, base) -> np.ndarray:
+    lib = load()
+    g, a = to_geometry(geom), to_aberr(base)
+    cnt = ctypes.c_int(0)
+    _check("ssb_bf_indices", lib.ssb_bf_indices(ctypes.byref(g), ctypes.byref(a), None, ctypes.byref(cnt)))
+    out = np.zeros(max(cnt.value, 1), dtype=np.int32)
+    _check("ssb_bf_indices", lib.ssb_bf_indices(ctypes.byref(g), ctypes.byref(a),
+                                                out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                                ctypes.byref(cnt)))
+    return out[:cnt.value]
+
+
+def band_indices(geom, qmin=0.2, qmax=0.9) -> np.ndarray:
+    lib = load()
+    g = to_geometry(geom)
+    cnt = ctypes.c_int(0)
+    _check("ssb_band_indices", lib.ssb_band_indices(ctypes.byref(g), qmin, qmax, None, ctypes.byref(cnt)))
+    out = np.zeros(max(cnt.value, 1), dtype=np.int32)
+    _check("ssb_band_indices", lib.ssb_band_indices(ctypes.byref(g), qmin, qmax,
+                                                    out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                                    ctypes.byref(cnt)))
+    return out[:cnt.value]
+
+
+def workspace_bytes(geom, n_bf, op, B=1, nq=1) -> int:
+    return int(load().ssb_workspace_bytes(ctypes.byref(to_geometry(geom)), int(n_bf), int(op), int(B), int(nq)))
+
+
+def launch_count() -> int:
+    return int(load().ssb_launch_count())
+
+
+# ----------------------------------------------------------------------------
+# device entry points (torch tensors on the current CUDA device)
+# ----------------------------------------------------------------------------
+
+def _workspace(nbytes, device):
+    import torch
+    # 256 extra bytes so the pointer can be rounded up to a 256-byte boundary
+    raw = torch.empty(int(nbytes) + 256, dtype=torch.uint8, device=device)
+    off = (-int(raw.data_ptr())) % 256
+    return raw, raw[off:off + int(nbytes)]
+
+
+class Workspace:
+    """A reusable device workspace (caller-owned scratch for the library)."""
+
+    def __init__(self, nbytes, device="cuda"):
+        self._raw, self.view = _workspace(max(int(nbytes), 256), device)
+        self.nbytes = int(nbytes)
+
+    def ptr(self):
+        return _ptr(self.view)
+
+
+def _dtype_code(frames):
+    import torch
+    if frames.dtype == torch.float32:
+        return SSB_F32
+    if frames.dtype in (torch.int16, torch.uint16 if hasattr(torch, "uint16") else torch.int16):
+        return SSB_U16
+    raise TypeError(f"frames must be float32 or 16-bit counts, got {frames.dtype}")
+
+
+def build_G(frames, geom, bf_idx_dev, G=None, ws=None, stream=None):
+    """G(q,k) half plane (complex64 [n_bf, n, n/2+1]) from device frames."""
+    import torch
+    lib = load()
+    g = to_geometry(geom)
+    n_bf = int(bf_idx_dev.numel())
+    if not frames.is_cuda or not bf_idx_dev.is_cuda:
+        raise ValueError("frames and bf_idx must be CUDA tensors")
+    if not frames.is_contiguous():
+        raise ValueError("frames must be contiguous")
+    if G is None:
+        G = torch.empty((n_bf, g.n, g.n // 2 + 1), dtype=torch.complex64, device=frames.device)
+    need = workspace_bytes(g, n_bf, OP_BUILD)
+    if ws is None:
+        ws = Workspace(need, frames.device)
+    _check("ssb_build_G", lib.ssb_build_G(_ptr(frames), _dtype_code(frames), ctypes.byref(g),
+                                          _ptr(bf_idx_dev), n_bf, _ptr(G), ws.ptr(),
+                                          ws.nbytes, _stream(stream)))
+    return G
+
+
+def reconstruct(G, geom, bf_idx_dev, aberr, O=None, N=None, phase=None, ws=None, stream=None):
+    """One reconstruction: returns (O complex64 [n, n/2+1], N int32 [n, n/2+1],
+    phase float32 [n, n])."""
+    import torch
+    lib = load()
+    g = to_geometry(geom)
+    a = to_aberr(aberr)
+    n_bf = int(bf_idx_dev.numel())
+    n, h = g.n, g.n // 2 + 1
+    dev = G.device
+    O = torch.empty((n, h), dtype=torch.complex64, device=dev) if O is None else O
+    N = torch.empty((n, h), dtype=torch.int32, device=dev) if N is None else N
+    phase = torch.empty((n, n), dtype=torch.float32, device=dev) if phase is None else phase
+    if ws is None:
+        ws = Workspace(workspace_bytes(g, n_bf, OP_RECON), dev)
+    _check("ssb_reconstruct", lib.ssb_reconstruct(_ptr(G), ctypes.byref(g), _ptr(bf_idx_dev), n_bf,
+                                                  ctypes.byref(a), _ptr(O), _ptr(N), _ptr(phase),
+                                                  ws.ptr(), ws.nbytes, _stream(stream)))
+    return O, N, phase
+
+
+def score_batch(G, geom, bf_idx_dev, sets, band_dev, O=None, N=None, score=None, ws=None, stream=None):
+    """Batched scoring of B <= 8 sets over a band list: returns
+    (O complex64 [B, nq], N int32 [B, nq], score float64 [B])."""
+    import torch
+    lib = load()
+    g = to_geometry(geom)
+    B = len(sets)
+    arr = (Aberr * max(B, 1))(*[to_aberr(s) for s in sets])
+    n_bf = int(bf_idx_dev.numel())
+    nq = int(band_dev.numel())
+    dev = G.device
+    O = torch.empty((B, nq), dtype=torch.complex64, device=dev) if O is None else O
+    N = torch.empty((B, nq), dtype=torch.int32, device=dev) if N is None else N
+    score = torch.empty((B,), dtype=torch.float64, device=dev) if score is None else score
+    if ws is None:
+        need = workspace_bytes(g, n_bf, OP_SCORE, B, nq)
+        if need == 0:
+            raise SSBError("ssb_workspace_bytes", SSB_INVALID_ARG, f"invalid sizes (B={B}, nq={nq})")
+        ws = Workspace(need, dev)
+    _check("ssb_score_batch", lib.ssb_score_batch(_ptr(G), ctypes.byref(g), _ptr(bf_idx_dev), n_bf, arr, B,
+                                                  _ptr(band_dev), nq, _ptr(O), _ptr(N), _ptr(score),
+                                                  ws.ptr(), ws.nbytes, _stream(stream)))
+    return O, N, score

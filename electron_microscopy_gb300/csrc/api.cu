@@ -1,0 +1,344 @@
+// api.cu -- the C ABI declared in include/ssb.h: argument checks, host-side
+// index sets, workspace layout and the launch sequence of each operation.
+#include <atomic>
+#include <cstdarg>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+
+#include "internal.cuh"
+
+namespace ssb {
+
+static thread_local char g_err[512] = "";
+static std::atomic<long long> g_launches{0};
+
+void count_launch(int k) { g_launches.fetch_add(k, std::memory_order_relaxed); }
+
+static int fail(int code, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+static int fail(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+static int cuda_fail(cudaError_t e, const char* where) {
+    return fail(SSB_CUDA_ERROR, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// IEEE double product with its own rounding, whatever the host compiler's
+// contraction settings (the BF predicate must match a plain float64 reading).
+static double mul_rn(double a, double b) {
+    volatile double r = a * b;
+    return r;
+}
+
+static bool is_pow2(int n) { return n > 0 && (n & (n - 1)) == 0; }
+
+static int check_geom(const ssb_geometry* g) {
+    if (!g) return fail(SSB_INVALID_ARG, "geometry is NULL");
+    if (g->det_y < 1 || g->det_x < 1) return fail(SSB_INVALID_ARG, "detector size must be >= 1");
+    if ((long long)g->det_y * g->det_x > (1LL << 30))
+        return fail(SSB_INVALID_ARG, "detector too large");
+    if (!(g->scan_step_A > 0) || !(g->det_pitch_invA > 0) || !(g->wavelength_A > 0) ||
+        !(g->semiangle_rad > 0))
+        return fail(SSB_INVALID_ARG, "scan step, detector pitch, wavelength and semi-angle must be > 0");
+    if (!std::isfinite(g->det_center_x) || !std::isfinite(g->det_center_y))
+        return fail(SSB_INVALID_ARG, "detector centre must be finite");
+    if (!is_pow2(g->n) || g->n < SSB_MIN_N || g->n > SSB_MAX_N)
+        return fail(SSB_UNSUPPORTED, "scan size n=%d must be a power of two in [%d, %d]", g->n, SSB_MIN_N,
+                    SSB_MAX_N);
+    return SSB_OK;
+}
+
+static int check_set(const ssb_aberr* a) {
+    const double* v = &a->C10;
+    for (int i = 0; i < 14; ++i)
+        if (!std::isfinite(v[i])) return fail(SSB_INVALID_ARG, "aberration value %d is not finite", i);
+    return SSB_OK;
+}
+
+// float32 constants of one aberration set (chi in turns, see internal.cuh)
+static SetParams set_params(const ssb_geometry* g, const ssb_aberr* a) {
+    const double lam = g->wavelength_A, l2 = lam * lam, l3 = l2 * lam;
+    SetParams p;
+    p.tx = (float)(a->tilt_x_rad / lam);
+    p.ty = (float)(a->tilt_y_rad / lam);
+    p.c[0] = (float)(lam * a->C10 / 2.0);
+    p.c[1] = (float)(lam * a->C12a / 2.0);
+    p.c[2] = (float)(lam * a->C12b);
+    p.c[3] = (float)(l2 * a->C21a / 3.0);
+    p.c[4] = (float)(l2 * a->C21b / 3.0);
+    p.c[5] = (float)(l2 * a->C23a / 3.0);
+    p.c[6] = (float)(l2 * a->C23b / 3.0);
+    p.c[7] = (float)(l3 * a->C30 / 4.0);
+    p.c[8] = (float)(l3 * a->C32a / 4.0);
+    p.c[9] = (float)(l3 * a->C32b / 2.0);
+    p.c[10] = (float)(l3 * a->C34a / 4.0);
+    p.c[11] = (float)(l3 * a->C34b);
+    return p;
+}
+
+static float aperture_r2(const ssb_geometry* g) {
+    const double r = g->semiangle_rad / g->wavelength_A;
+    return (float)mul_rn(r, r);
+}
+
+// ---------------------------------------------------------------------------
+// workspace layout
+// ---------------------------------------------------------------------------
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Number of k-splits of the reduction: enough CTAs for ~2 waves on a
+// 152-SM part at 8 resident CTAs each; depends only on (nq, n_bf) so that the
+// summation order is the same for every B.
+static int red_splits(int nq, int n_bf) {
+    const int bx = (nq + 255) / 256;
+    int s = (2 * 152 * 8 + bx - 1) / bx;
+    if (s < 1) s = 1;
+    if (s > 64) s = 64;
+    const int max_s = (n_bf + 15) / 16;  // at least 16 k per split
+    if (s > max_s) s = max_s;
+    if (s < 1) s = 1;
+    return s;
+}
+
+struct WsLayout {
+    size_t tw, ktab, chik, amask, Opart, Npart, dcpart, Y, total;
+};
+
+static WsLayout layout(const ssb_geometry* g, int n_bf, int op, int B, int nq) {
+    WsLayout L{};
+    const int n = g->n, H = n / 2 + 1;
+    size_t off = 0;
+    L.tw = off;
+    off += align256((size_t)n * sizeof(float2));
+    if (op == SSB_OP_BUILD) {
+        L.total = off;
+        return L;
+    }
+    if (op == SSB_OP_RECON) {
+        B = 1;
+        nq = n * H;
+    }
+    const int ns = red_splits(nq, n_bf);
+    L.ktab = off;
+    off += align256((size_t)n_bf * sizeof(float4));
+    L.chik = off;
+    off += align256((size_t)B * n_bf * sizeof(float));
+    L.amask = off;
+    off += align256((size_t)n_bf * sizeof(uint32_t));
+    L.Opart = off;
+    off += align256((size_t)ns * B * nq * sizeof(float2));
+    L.Npart = off;
+    off += align256((size_t)ns * B * nq * sizeof(int));
+    L.dcpart = off;
+    off += align256((size_t)ns * sizeof(double));
+    if (op == SSB_OP_RECON) {
+        L.Y = off;
+        off += align256((size_t)n * H * sizeof(float2));
+    }
+    L.total = off;
+    return L;
+}
+
+template <typename T>
+static T* at(void* ws, size_t off) {
+    return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+static int check_ws(void* ws, size_t ws_bytes, size_t need) {
+    if (!ws) return fail(SSB_INVALID_ARG, "workspace is NULL");
+    if (reinterpret_cast<uintptr_t>(ws) & 255) return fail(SSB_INVALID_ARG, "workspace must be 256-byte aligned");
+    if (ws_bytes < need)
+        return fail(SSB_WORKSPACE_TOO_SMALL, "workspace has %zu bytes, needs %zu", ws_bytes, need);
+    return SSB_OK;
+}
+
+// shared by reconstruct and score: k tables, reduction, finalize
+static int run_reduction(const void* G_dev, const ssb_geometry* g, const int32_t* bf_idx, int n_bf,
+                         const SetBatch& sb, const int32_t* qlist, int nq, float2* O, int32_t* N,
+                         void* ws, const WsLayout& Lw, int want_dc, cudaStream_t st) {
+    cudaError_t e;
+    float4* ktab = at<float4>(ws, Lw.ktab);
+    float* chik = at<float>(ws, Lw.chik);
+    uint32_t* amask = at<uint32_t>(ws, Lw.amask);
+    if ((e = launch_prep(bf_idx, n_bf, g->det_x, g->det_center_y, g->det_center_x, g->det_pitch_invA, sb,
+                         ktab, chik, amask, st)) != cudaSuccess)
+        return cuda_fail(e, "prep");
+    RedLaunch P{};
+    P.G = static_cast<const float2*>(G_dev);
+    P.n = g->n;
+    P.n_bf = n_bf;
+    P.nq = nq;
+    P.nsplit = red_splits(nq, n_bf);
+    P.kps = (n_bf + P.nsplit - 1) / P.nsplit;
+    P.dq = 1.0 / ((double)g->n * g->scan_step_A);
+    P.qlist = qlist;
+    P.ktab = ktab;
+    P.chik = chik;
+    P.amask = amask;
+    P.Opart = at<float2>(ws, Lw.Opart);
+    P.Npart = at<int>(ws, Lw.Npart);
+    P.dcpart = at<double>(ws, Lw.dcpart);
+    P.want_dc = want_dc;
+    if ((e = launch_reduce(P, sb, st)) != cudaSuccess) return cuda_fail(e, "reduce");
+    if ((e = launch_finalize(P.Opart, P.Npart, P.nsplit, sb.B, nq, O, N, st)) != cudaSuccess)
+        return cuda_fail(e, "finalize");
+    return SSB_OK;
+}
+
+}  // namespace ssb
+
+using namespace ssb;
+
+extern "C" {
+
+const char* ssb_last_error(void) { return g_err; }
+
+long long ssb_launch_count(void) { return g_launches.load(); }
+
+int ssb_bf_indices(const ssb_geometry* geom, const ssb_aberr* base, int32_t* out, int* n_bf) {
+    int rc;
+    if ((rc = check_geom(geom)) != SSB_OK) return rc;
+    if (!base || !n_bf) return fail(SSB_INVALID_ARG, "base set and n_bf must not be NULL");
+    if ((rc = check_set(base)) != SSB_OK) return rc;
+    const double lam = geom->wavelength_A, dk = geom->det_pitch_invA;
+    const double r = geom->semiangle_rad / lam;
+    const double r2 = mul_rn(r, r);
+    const double tkx = base->tilt_x_rad / lam, tky = base->tilt_y_rad / lam;
+    int count = 0;
+    for (int i = 0; i < geom->det_y; ++i) {
+        const double ey = mul_rn((double)i - geom->det_center_y, dk) - tky;
+        for (int j = 0; j < geom->det_x; ++j) {
+            const double ex = mul_rn((double)j - geom->det_center_x, dk) - tkx;
+            if (mul_rn(ex, ex) + mul_rn(ey, ey) <= r2) {
+                if (out) out[count] = i * geom->det_x + j;
+                ++count;
+            }
+        }
+    }
+    *n_bf = count;
+    g_err[0] = 0;
+    return SSB_OK;
+}
+
+int ssb_band_indices(const ssb_geometry* geom, double qmin, double qmax, int32_t* out, int* nq) {
+    int rc;
+    if ((rc = check_geom(geom)) != SSB_OK) return rc;
+    if (!nq) return fail(SSB_INVALID_ARG, "nq must not be NULL");
+    if (!(qmin >= 0) || !(qmax >= qmin)) return fail(SSB_INVALID_ARG, "need 0 <= qmin <= qmax");
+    const int n = geom->n, H = n / 2 + 1;
+    const double dq = 1.0 / ((double)n * geom->scan_step_A);
+    const double lo = mul_rn(qmin / dq, qmin / dq);
+    const double hi = mul_rn(qmax / dq, qmax / dq);
+    int count = 0;
+    for (int row = 0; row < n; ++row) {
+        const long long fy = row < n / 2 ? row : row - n;
+        for (int col = 0; col < H; ++col) {
+            const double r2 = (double)(fy * fy + (long long)col * col);
+            if (r2 >= lo && r2 <= hi) {
+                if (out) out[count] = row * H + col;
+                ++count;
+            }
+        }
+    }
+    *nq = count;
+    g_err[0] = 0;
+    return SSB_OK;
+}
+
+size_t ssb_workspace_bytes(const ssb_geometry* geom, int n_bf, int op, int B, int nq) {
+    if (check_geom(geom) != SSB_OK) return 0;
+    if (n_bf < 1) return 0;
+    if (op == SSB_OP_SCORE && (B < 1 || B > SSB_MAX_SETS || nq < 1)) return 0;
+    if (op != SSB_OP_BUILD && op != SSB_OP_RECON && op != SSB_OP_SCORE) return 0;
+    return layout(geom, n_bf, op, B, nq).total;
+}
+
+int ssb_build_G(const void* frames, int dtype, const ssb_geometry* geom, const int32_t* bf_idx_dev,
+                int n_bf, void* G_dev, void* ws, size_t ws_bytes, void* stream) {
+    int rc;
+    if ((rc = check_geom(geom)) != SSB_OK) return rc;
+    if (!frames || !bf_idx_dev || !G_dev) return fail(SSB_INVALID_ARG, "frames, bf_idx and G must not be NULL");
+    if (dtype != SSB_U16 && dtype != SSB_F32) return fail(SSB_INVALID_ARG, "dtype must be SSB_U16 or SSB_F32");
+    if (n_bf < 1 || (long long)n_bf > (long long)geom->det_y * geom->det_x)
+        return fail(SSB_INVALID_ARG, "n_bf=%d out of range", n_bf);
+    const WsLayout Lw = layout(geom, n_bf, SSB_OP_BUILD, 1, 1);
+    if ((rc = check_ws(ws, ws_bytes, Lw.total)) != SSB_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    float2* tw = at<float2>(ws, Lw.tw);
+    cudaError_t e;
+    if ((e = launch_twiddles(tw, geom->n, st)) != cudaSuccess) return cuda_fail(e, "twiddles");
+    if ((e = launch_build(frames, dtype, geom->n, geom->det_y * geom->det_x, bf_idx_dev, n_bf,
+                          static_cast<float2*>(G_dev), tw, st)) != cudaSuccess)
+        return cuda_fail(e, "build");
+    g_err[0] = 0;
+    return SSB_OK;
+}
+
+int ssb_reconstruct(const void* G_dev, const ssb_geometry* geom, const int32_t* bf_idx_dev, int n_bf,
+                    const ssb_aberr* set, void* O_dev, int32_t* N_dev, float* phase_dev, void* ws,
+                    size_t ws_bytes, void* stream) {
+    int rc;
+    if ((rc = check_geom(geom)) != SSB_OK) return rc;
+    if (!G_dev || !bf_idx_dev || !set || !O_dev || !N_dev || !phase_dev)
+        return fail(SSB_INVALID_ARG, "G, bf_idx, set, O, N and phase must not be NULL");
+    if (n_bf < 1 || (long long)n_bf > (long long)geom->det_y * geom->det_x)
+        return fail(SSB_INVALID_ARG, "n_bf=%d out of range", n_bf);
+    if ((rc = check_set(set)) != SSB_OK) return rc;
+    const WsLayout Lw = layout(geom, n_bf, SSB_OP_RECON, 1, 0);
+    if ((rc = check_ws(ws, ws_bytes, Lw.total)) != SSB_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    SetBatch sb{};
+    sb.B = 1;
+    sb.r2 = aperture_r2(geom);
+    sb.s[0] = set_params(geom, set);
+    const int n = geom->n, nq = n * (n / 2 + 1);
+    float2* tw = at<float2>(ws, Lw.tw);
+    cudaError_t e;
+    if ((e = launch_twiddles(tw, n, st)) != cudaSuccess) return cuda_fail(e, "twiddles");
+    if ((rc = run_reduction(G_dev, geom, bf_idx_dev, n_bf, sb, nullptr, nq, static_cast<float2*>(O_dev), N_dev,
+                            ws, Lw, 1, st)) != SSB_OK)
+        return rc;
+    if ((e = launch_phase(static_cast<const float2*>(O_dev), N_dev, at<double>(ws, Lw.dcpart),
+                          red_splits(nq, n_bf), n_bf, n, at<float2>(ws, Lw.Y), tw, phase_dev, st)) != cudaSuccess)
+        return cuda_fail(e, "phase");
+    g_err[0] = 0;
+    return SSB_OK;
+}
+
+int ssb_score_batch(const void* G_dev, const ssb_geometry* geom, const int32_t* bf_idx_dev, int n_bf,
+                    const ssb_aberr* sets, int B, const int32_t* band_dev, int nq, void* O_dev,
+                    int32_t* N_dev, double* score_dev, void* ws, size_t ws_bytes, void* stream) {
+    int rc;
+    if ((rc = check_geom(geom)) != SSB_OK) return rc;
+    if (!G_dev || !bf_idx_dev || !sets || !band_dev || !O_dev || !N_dev || !score_dev)
+        return fail(SSB_INVALID_ARG, "G, bf_idx, sets, band, O, N and score must not be NULL");
+    if (B < 1 || B > SSB_MAX_SETS) return fail(SSB_UNSUPPORTED, "B=%d not in [1, %d]", B, SSB_MAX_SETS);
+    if (n_bf < 1 || (long long)n_bf > (long long)geom->det_y * geom->det_x)
+        return fail(SSB_INVALID_ARG, "n_bf=%d out of range", n_bf);
+    if (nq < 1 || (long long)nq > (long long)geom->n * (geom->n / 2 + 1))
+        return fail(SSB_INVALID_ARG, "nq=%d out of range", nq);
+    for (int s = 0; s < B; ++s)
+        if ((rc = check_set(&sets[s])) != SSB_OK) return rc;
+    const WsLayout Lw = layout(geom, n_bf, SSB_OP_SCORE, B, nq);
+    if ((rc = check_ws(ws, ws_bytes, Lw.total)) != SSB_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    SetBatch sb{};
+    sb.B = B;
+    sb.r2 = aperture_r2(geom);
+    for (int s = 0; s < B; ++s) sb.s[s] = set_params(geom, &sets[s]);
+    if ((rc = run_reduction(G_dev, geom, bf_idx_dev, n_bf, sb, band_dev, nq, static_cast<float2*>(O_dev), N_dev,
+                            ws, Lw, 0, st)) != SSB_OK)
+        return rc;
+    cudaError_t e;
+    if ((e = launch_score(static_cast<const float2*>(O_dev), N_dev, B, nq, score_dev, st)) != cudaSuccess)
+        return cuda_fail(e, "score");
+    g_err[0] = 0;
+    return SSB_OK;
+}
+
+}  // extern "C"

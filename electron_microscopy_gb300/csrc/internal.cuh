@@ -1,0 +1,224 @@
+// internal.cuh -- device building blocks shared by the SSB kernels (not part of the C ABI).
+//
+// * Complex helpers on float2.
+// * A warp-level in-place Stockham FFT (radix 8/4/2) on a shared-memory row:
+//   each pass reads every point of the row into registers, applies the
+//   twiddles and a radix-R butterfly, and writes the autosorted output back
+//   (the Stockham formulation of Govindaraju et al., "High Performance
+//   Discrete Fourier Transforms on Graphics Processors", SC 2008).  Twiddles
+//   come from a per-call table W[m] = exp(-2 pi i m / n), m < n, rounded once
+//   from double precision.
+// * The aberration polynomial chi/(2 pi) in Cartesian form and the float32
+//   aperture test whose operation order is part of the library contract.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ssb.h"
+
+namespace ssb {
+
+// ---------------------------------------------------------------------------
+// complex helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float2 cadd(float2 a, float2 b) { return make_float2(a.x + b.x, a.y + b.y); }
+__device__ __forceinline__ float2 csub(float2 a, float2 b) { return make_float2(a.x - b.x, a.y - b.y); }
+__device__ __forceinline__ float2 cmul(float2 a, float2 b) {
+    return make_float2(a.x * b.x - a.y * b.y, a.x * b.y + a.y * b.x);
+}
+__device__ __forceinline__ float2 cconj(float2 a) { return make_float2(a.x, -a.y); }
+// multiply by -i
+__device__ __forceinline__ float2 cmul_mi(float2 a) { return make_float2(a.y, -a.x); }
+// multiply by +i
+__device__ __forceinline__ float2 cmul_pi(float2 a) { return make_float2(-a.y, a.x); }
+
+// ---------------------------------------------------------------------------
+// radix-R forward DFT in registers, X[k] = sum_m v[m] exp(-2 pi i m k / R)
+// ---------------------------------------------------------------------------
+template <int R> struct Dft;
+
+template <> struct Dft<2> {
+    static __device__ __forceinline__ void run(float2* v) {
+        float2 a = v[0], b = v[1];
+        v[0] = cadd(a, b);
+        v[1] = csub(a, b);
+    }
+};
+
+template <> struct Dft<4> {
+    static __device__ __forceinline__ void run(float2* v) {
+        float2 t0 = cadd(v[0], v[2]), t1 = csub(v[0], v[2]);
+        float2 t2 = cadd(v[1], v[3]), t3 = cmul_mi(csub(v[1], v[3]));
+        v[0] = cadd(t0, t2);
+        v[2] = csub(t0, t2);
+        v[1] = cadd(t1, t3);
+        v[3] = csub(t1, t3);
+    }
+};
+
+template <> struct Dft<8> {
+    // split into a radix-2 stage (m, m+4), twiddles W8^m on the difference
+    // half, then two radix-4 DFTs giving the even and odd outputs.
+    static __device__ __forceinline__ void run(float2* v) {
+        const float h = 0.70710678118654752f;  // 1/sqrt(2)
+        float2 a[4], b[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            a[m] = cadd(v[m], v[m + 4]);
+            b[m] = csub(v[m], v[m + 4]);
+        }
+        // b1 *= (1 - i)/sqrt2 ; b2 *= -i ; b3 *= (-1 - i)/sqrt2
+        b[1] = make_float2(h * (b[1].x + b[1].y), h * (b[1].y - b[1].x));
+        b[2] = cmul_mi(b[2]);
+        b[3] = make_float2(h * (b[3].y - b[3].x), -h * (b[3].x + b[3].y));
+        Dft<4>::run(a);
+        Dft<4>::run(b);
+        v[0] = a[0]; v[2] = a[1]; v[4] = a[2]; v[6] = a[3];
+        v[1] = b[0]; v[3] = b[1]; v[5] = b[2]; v[7] = b[3];
+    }
+};
+
+// ---------------------------------------------------------------------------
+// warp-level in-place Stockham pass over a row of L points in shared memory.
+// NS: span of the sub-transforms already done; TWS: stride into the
+// length-n twiddle table (n / L).
+// ---------------------------------------------------------------------------
+template <int L, int R, int NS, int TWS>
+__device__ __forceinline__ void stockham_pass(float2* buf, const float2* tw, int lane) {
+    constexpr int NB = L / R;
+    constexpr int PER = (NB + 31) / 32;
+    float2 v[PER][R];
+#pragma unroll
+    for (int t = 0; t < PER; ++t) {
+        const int j = lane + 32 * t;
+        if (NB >= 32 || j < NB) {
+#pragma unroll
+            for (int r = 0; r < R; ++r) v[t][r] = buf[j + r * NB];
+        }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int t = 0; t < PER; ++t) {
+        const int j = lane + 32 * t;
+        if (NB >= 32 || j < NB) {
+            const int k = j & (NS - 1);
+            if (NS > 1) {
+#pragma unroll
+                for (int r = 1; r < R; ++r)
+                    v[t][r] = cmul(v[t][r], tw[(k * r * (L / (NS * R))) * TWS]);
+            }
+            Dft<R>::run(v[t]);
+            const int base = (j - k) * R + k;
+#pragma unroll
+            for (int r = 0; r < R; ++r) buf[base + r * NS] = v[t][r];
+        }
+    }
+    __syncwarp();
+}
+
+template <int L, int NS, int TWS>
+__device__ __forceinline__ void fft_passes(float2* buf, const float2* tw, int lane) {
+    if constexpr (NS < L) {
+        constexpr int REM = L / NS;
+        constexpr int R = (REM >= 8) ? 8 : REM;
+        stockham_pass<L, R, NS, TWS>(buf, tw, lane);
+        fft_passes<L, NS * R, TWS>(buf, tw, lane);
+    }
+}
+
+// Forward complex FFT (exp(-2 pi i ...)) of length L, in place, by one warp.
+template <int L, int TWS>
+__device__ __forceinline__ void fft_warp(float2* buf, const float2* tw, int lane) {
+    fft_passes<L, 1, TWS>(buf, tw, lane);
+}
+
+// ---------------------------------------------------------------------------
+// aberration sets
+// ---------------------------------------------------------------------------
+// chi/(2 pi) in turns as a polynomial of v = (vx, vy) (1/Angstrom):
+//   xx = vx^2, yy = vy^2, s = xx + yy, u = xx - yy, p = vx vy
+//   deg2 = c0 s + c1 u + c2 p
+//   deg3 = s (c3 vx + c4 vy) + c5 vx (xx - 3 yy) + c6 vy (3 xx - yy)
+//   deg4 = s (c7 s + c8 u + c9 p) + c10 (u^2 - 4 p^2) + c11 u p
+// with c0 = lam C10/2, c1 = lam C12a/2, c2 = lam C12b, c3 = lam^2 C21a/3,
+// c4 = lam^2 C21b/3, c5 = lam^2 C23a/3, c6 = lam^2 C23b/3, c7 = lam^3 C30/4,
+// c8 = lam^3 C32a/4, c9 = lam^3 C32b/2, c10 = lam^3 C34a/4, c11 = lam^3 C34b.
+// (theta^m cos(n phi), theta^m sin(n phi) written through Re/Im of
+// (vx + i vy)^n; the division-free Cartesian form the tilt-speed page uses.)
+struct SetParams {
+    float tx, ty;   // float32(k_t)
+    float c[12];
+};
+
+struct SetBatch {
+    SetParams s[SSB_MAX_SETS];
+    float r2;       // float32((alpha/lambda)^2)
+    int B;
+};
+
+// Every operation explicitly rounded so that the value is identical in every
+// kernel that evaluates it (k-only tables, single-set and batched passes).
+__device__ __forceinline__ float chi_turns(const float* c, float vx, float vy) {
+    const float xx = __fmul_rn(vx, vx), yy = __fmul_rn(vy, vy);
+    const float s = __fadd_rn(xx, yy), u = __fsub_rn(xx, yy), p = __fmul_rn(vx, vy);
+    float d2 = __fmaf_rn(c[2], p, __fmaf_rn(c[1], u, __fmul_rn(c[0], s)));
+    const float t5 = __fmul_rn(vx, __fmaf_rn(-3.0f, yy, xx));
+    const float t6 = __fmul_rn(vy, __fmaf_rn(3.0f, xx, -yy));
+    float d3 = __fmul_rn(s, __fmaf_rn(c[4], vy, __fmul_rn(c[3], vx)));
+    d3 = __fmaf_rn(c[6], t6, __fmaf_rn(c[5], t5, d3));
+    const float q4 = __fmaf_rn(u, u, __fmul_rn(-4.0f, __fmul_rn(p, p)));
+    float d4 = __fmul_rn(s, __fmaf_rn(c[9], p, __fmaf_rn(c[8], u, __fmul_rn(c[7], s))));
+    d4 = __fmaf_rn(c[11], __fmul_rn(u, p), __fmaf_rn(c[10], q4, d4));
+    return __fadd_rn(__fadd_rn(d2, d3), d4);
+}
+
+// Aperture test, float32 contract: dx = px - tx; dy = py - ty;
+// d2 = dx*dx + dy*dy (each rounded separately); inside iff d2 <= r2.
+__device__ __forceinline__ bool aperture_f32(float px, float py, float tx, float ty, float r2,
+                                             float* dxo, float* dyo) {
+    const float dx = __fsub_rn(px, tx), dy = __fsub_rn(py, ty);
+    const float d2 = __fadd_rn(__fmul_rn(dx, dx), __fmul_rn(dy, dy));
+    *dxo = dx;
+    *dyo = dy;
+    return d2 <= r2;
+}
+
+// ---------------------------------------------------------------------------
+// host-side launchers (defined in build.cu / reduce.cu); return cudaError_t
+// ---------------------------------------------------------------------------
+cudaError_t launch_twiddles(float2* tw, int n, cudaStream_t st);
+cudaError_t launch_build(const void* frames, int dtype, int n, int det_pix,
+                         const int32_t* bf_idx, int n_bf, float2* G, const float2* tw,
+                         cudaStream_t st);
+
+struct RedLaunch {
+    const float2* G;
+    int n, n_bf, nq, nsplit, kps;
+    double dq;
+    const int32_t* qlist;   // null: identity over the half plane
+    float4* ktab;
+    float* chik;            // [B][n_bf]
+    uint32_t* amask;
+    float2* Opart;          // [nsplit][B][nq]
+    int* Npart;             // [nsplit][B][nq]
+    double* dcpart;         // [nsplit]
+    int want_dc;
+};
+
+cudaError_t launch_prep(const int32_t* bf_idx, int n_bf, int det_x, double cy, double cx, double dk,
+                        const SetBatch& sb, float4* ktab, float* chik, uint32_t* amask,
+                        cudaStream_t st);
+cudaError_t launch_reduce(const RedLaunch& L, const SetBatch& sb, cudaStream_t st);
+cudaError_t launch_finalize(const float2* Opart, const int* Npart, int nsplit, int B, int nq,
+                            float2* O, int32_t* N, cudaStream_t st);
+cudaError_t launch_phase(const float2* O, const int32_t* N, const double* dcpart, int nsplit,
+                         int n_bf, int n, float2* Y, const float2* tw, float* phase,
+                         cudaStream_t st);
+cudaError_t launch_score(const float2* O, const int32_t* N, int B, int nq, double* score,
+                         cudaStream_t st);
+
+// launch bookkeeping (api.cu)
+void count_launch(int k = 1);
+
+}  // namespace ssb

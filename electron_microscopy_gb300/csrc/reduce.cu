@@ -1,0 +1,334 @@
+// reduce.cu -- trotter-masked, aberration-weighted reduction over bright-field
+// pixels, spectrum assembly + complex-to-real inverse + atan2, and the band score.
+//
+// Per (q, k, set) term (quantem.gpu "Tilt-corrected SSB on CUDA", sections
+// "Where the time went" and "Changes"): three aperture tests decide the
+// trotter class; a single-overlap pixel adds G(q,k) w to O(q) and 1 to N(q),
+// with w = exp(-i(chi(k) - chi(k-q))) on T- and -exp(+i(chi(k) - chi(k+q))) on
+// T+.  Per-set accumulators live in registers (the set loop is unrolled to a
+// compile-time maximum with a uniform b < B guard); chi(k) and the aperture at
+// k are computed once per call into k-only tables.
+//
+// Thread <-> q layout: consecutive lanes own consecutive half-plane entries,
+// so each k step reads G[k][q..q+31] as one coalesced 256-byte segment and the
+// sum over k needs no cross-thread reduction.  The k range is split across
+// grid.y; partial sums are added in a fixed order by the finalize kernel, so
+// results are deterministic and independent of the number of sets B.
+#include "internal.cuh"
+
+namespace ssb {
+
+// ---------------------------------------------------------------------------
+// k-only tables: float32 k, aperture bit per set, chi_s(k) in turns
+// ---------------------------------------------------------------------------
+__global__ void prep_kernel(const int32_t* __restrict__ bf_idx, int n_bf, int det_x, double cy,
+                            double cx, double dk, SetBatch sb, float4* __restrict__ ktab,
+                            float* __restrict__ chik, uint32_t* __restrict__ amask) {
+    const int k = blockIdx.x * blockDim.x + threadIdx.x;
+    if (k >= n_bf) return;
+    const int idx = bf_idx[k];
+    const int i = idx / det_x, j = idx - i * det_x;
+    const float kx = __double2float_rn(__dmul_rn(__dsub_rn((double)j, cx), dk));
+    const float ky = __double2float_rn(__dmul_rn(__dsub_rn((double)i, cy), dk));
+    ktab[k] = make_float4(kx, ky, 0.f, 0.f);
+    uint32_t bits = 0;
+    for (int s = 0; s < sb.B; ++s) {
+        float vx, vy;
+        const bool a = aperture_f32(kx, ky, sb.s[s].tx, sb.s[s].ty, sb.r2, &vx, &vy);
+        bits |= (a ? 1u : 0u) << s;
+        chik[(size_t)s * n_bf + k] = a ? chi_turns(sb.s[s].c, vx, vy) : 0.f;
+    }
+    amask[k] = bits;
+}
+
+cudaError_t launch_prep(const int32_t* bf_idx, int n_bf, int det_x, double cy, double cx, double dk,
+                        const SetBatch& sb, float4* ktab, float* chik, uint32_t* amask,
+                        cudaStream_t st) {
+    prep_kernel<<<(n_bf + 255) / 256, 256, 0, st>>>(bf_idx, n_bf, det_x, cy, cx, dk, sb, ktab, chik,
+                                                    amask);
+    count_launch();
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// fused reduction
+// ---------------------------------------------------------------------------
+constexpr int kRedThreads = 256;
+
+template <int MAXB>
+__global__ void __launch_bounds__(kRedThreads)
+reduce_kernel(RedLaunch P, SetBatch sb) {
+    const int qi = blockIdx.x * kRedThreads + threadIdx.x;
+    const int split = blockIdx.y;
+    const int kb = split * P.kps;
+    const int ke = min(P.n_bf, kb + P.kps);
+    const int H = P.n / 2 + 1;
+    const bool valid = qi < P.nq;
+    const int e = valid ? (P.qlist ? P.qlist[qi] : qi) : 0;
+    const int row = e / H, col = e - row * H;
+    const int fy = row < P.n / 2 ? row : row - P.n;
+    const float qx = __double2float_rn(__dmul_rn((double)col, P.dq));
+    const float qy = __double2float_rn(__dmul_rn((double)fy, P.dq));
+
+    float2 acc[MAXB];
+    int cnt[MAXB];
+#pragma unroll
+    for (int s = 0; s < MAXB; ++s) {
+        acc[s] = make_float2(0.f, 0.f);
+        cnt[s] = 0;
+    }
+    double dc = 0.0;
+    const bool do_dc = P.want_dc && valid && e == 0;
+    const size_t plane = (size_t)P.n * H;
+    const float2* gp = P.G + e;
+
+    for (int k = kb; k < ke; ++k) {
+        const float2 g = valid ? __ldg(gp + (size_t)k * plane) : make_float2(0.f, 0.f);
+        const float4 kk = __ldg(P.ktab + k);
+        const uint32_t am = __ldg(P.amask + k);
+        const float mx = __fsub_rn(kk.x, qx), my = __fsub_rn(kk.y, qy);
+        const float px = __fadd_rn(kk.x, qx), py = __fadd_rn(kk.y, qy);
+        if (do_dc) dc += (double)g.x;
+#pragma unroll
+        for (int s = 0; s < MAXB; ++s) {
+            if (s < sb.B && ((am >> s) & 1u)) {
+                float mvx, mvy, pvx, pvy;
+                const bool m = aperture_f32(mx, my, sb.s[s].tx, sb.s[s].ty, sb.r2, &mvx, &mvy);
+                const bool p = aperture_f32(px, py, sb.s[s].tx, sb.s[s].ty, sb.r2, &pvx, &pvy);
+                if (m != p) {
+                    const float vx = m ? mvx : pvx, vy = m ? mvy : pvy;
+                    const float cq = chi_turns(sb.s[s].c, vx, vy);
+                    const float d = __fsub_rn(__ldg(P.chik + (size_t)s * P.n_bf + k), cq);
+                    const float r = __fsub_rn(d, rintf(d));
+                    float sn, cs;
+                    sincospif(__fmul_rn(2.0f, r), &sn, &cs);
+                    // T-: w = (cos, -sin); T+: w = (-cos, -sin)
+                    const float wr = m ? cs : -cs, wi = -sn;
+                    const float re = __fmaf_rn(g.x, wr, __fmul_rn(-g.y, wi));
+                    const float im = __fmaf_rn(g.x, wi, __fmul_rn(g.y, wr));
+                    acc[s].x = __fadd_rn(acc[s].x, re);
+                    acc[s].y = __fadd_rn(acc[s].y, im);
+                    cnt[s] += 1;
+                }
+            }
+        }
+    }
+    if (valid) {
+#pragma unroll
+        for (int s = 0; s < MAXB; ++s) {
+            if (s < sb.B) {
+                const size_t o = ((size_t)split * sb.B + s) * P.nq + qi;
+                P.Opart[o] = acc[s];
+                P.Npart[o] = cnt[s];
+            }
+        }
+    }
+    if (do_dc) P.dcpart[split] = dc;
+}
+
+cudaError_t launch_reduce(const RedLaunch& P, const SetBatch& sb, cudaStream_t st) {
+    dim3 grid((P.nq + kRedThreads - 1) / kRedThreads, P.nsplit);
+    if (sb.B == 1)
+        reduce_kernel<1><<<grid, kRedThreads, 0, st>>>(P, sb);
+    else if (sb.B == 2)
+        reduce_kernel<2><<<grid, kRedThreads, 0, st>>>(P, sb);
+    else if (sb.B <= 4)
+        reduce_kernel<4><<<grid, kRedThreads, 0, st>>>(P, sb);
+    else
+        reduce_kernel<8><<<grid, kRedThreads, 0, st>>>(P, sb);
+    count_launch();
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// partial sums -> O, N (fixed order over splits)
+// ---------------------------------------------------------------------------
+__global__ void finalize_kernel(const float2* __restrict__ Opart, const int* __restrict__ Npart,
+                                int nsplit, int B, int nq, float2* __restrict__ O,
+                                int32_t* __restrict__ N) {
+    const size_t t = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const size_t total = (size_t)B * nq;
+    if (t >= total) return;
+    float2 a = Opart[t];
+    int c = Npart[t];
+    for (int sp = 1; sp < nsplit; ++sp) {
+        const float2 v = Opart[(size_t)sp * total + t];
+        a.x = __fadd_rn(a.x, v.x);
+        a.y = __fadd_rn(a.y, v.y);
+        c += Npart[(size_t)sp * total + t];
+    }
+    O[t] = a;
+    N[t] = c;
+}
+
+cudaError_t launch_finalize(const float2* Opart, const int* Npart, int nsplit, int B, int nq,
+                            float2* O, int32_t* N, cudaStream_t st) {
+    const size_t total = (size_t)B * nq;
+    finalize_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(Opart, Npart, nsplit, B, nq, O, N);
+    count_launch();
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// phase image: S = O/N, Nyquist row/column and DC zeroed, B = -i S,
+// y = inverse C2C along q_y (unnormalised), b = C2R along q_x (numpy irfft
+// semantics), b /= n^2, phase = atan2(b, a), a = mean_k G(0,k) / n^2
+// ---------------------------------------------------------------------------
+constexpr int kPhaseThreads = 256;
+
+template <int N>
+__global__ void __launch_bounds__(kPhaseThreads)
+c2r_cols_kernel(const float2* __restrict__ O, const int32_t* __restrict__ Nn, float2* __restrict__ Y,
+                const float2* __restrict__ twg) {
+    constexpr int H = N / 2 + 1;
+    constexpr int CW = (N / 2 >= 16) ? 16 : N / 2;
+    constexpr int NG = (N / 2) / CW;
+    constexpr int CS = N + 1;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    float2* tw = reinterpret_cast<float2*>(smem_raw);
+    float2* cols = tw + N;
+    const int g = blockIdx.x;
+    const int c0 = g * CW;
+    const int nc = CW + ((g == NG - 1) ? 1 : 0);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    constexpr int NW = kPhaseThreads / 32;
+    for (int m = threadIdx.x; m < N; m += kPhaseThreads) tw[m] = twg[m];
+    for (int idx = threadIdx.x; idx < N * nc; idx += kPhaseThreads) {
+        const int row = idx / nc, c = idx - row * nc;
+        const int col = c0 + c;
+        const int e = row * H + col;
+        float2 b = make_float2(0.f, 0.f);
+        const int cnt = Nn[e];
+        if (cnt > 0 && row != N / 2 && col != N / 2 && e != 0) {
+            const float2 o = O[e];
+            const float sx = __fdiv_rn(o.x, (float)cnt), sy = __fdiv_rn(o.y, (float)cnt);
+            b = make_float2(sy, -sx);  // -i S
+        }
+        cols[c * CS + row] = cconj(b);  // inverse via conj(FFT(conj(.)))
+    }
+    __syncthreads();
+    for (int c = warp; c < nc; c += NW) fft_warp<N, 1>(cols + c * CS, tw, lane);
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < N * nc; idx += kPhaseThreads) {
+        const int row = idx / nc, c = idx - row * nc;
+        Y[(size_t)row * H + c0 + c] = cconj(cols[c * CS + row]);
+    }
+}
+
+template <int N>
+__global__ void __launch_bounds__(kPhaseThreads)
+c2r_rows_kernel(const float2* __restrict__ Y, const double* __restrict__ dcpart, int nsplit, int n_bf,
+                const float2* __restrict__ twg, float* __restrict__ phase) {
+    constexpr int L = N / 2;
+    constexpr int H = N / 2 + 1;
+    constexpr int RPB = kPhaseThreads / 32;  // rows per block, one warp each
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    float2* tw = reinterpret_cast<float2*>(smem_raw);
+    float2* zs = tw + N;  // RPB rows of L points
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int m = threadIdx.x; m < N; m += kPhaseThreads) tw[m] = twg[m];
+    double dc = 0.0;
+    for (int sp = 0; sp < nsplit; ++sp) dc += dcpart[sp];
+    const float a = (float)(dc / (double)n_bf / ((double)N * (double)N));
+    __syncthreads();
+    const int row = blockIdx.x * RPB + warp;
+    if (row >= N) return;
+    const float2* y = Y + (size_t)row * H;
+    float2* z = zs + warp * L;
+    // Z[k] = E[k] + i O[k], E = X[k] + conj X[L-k], O = (X[k] - conj X[L-k]) W^-k,
+    // with the imaginary parts of X[0] and X[L] dropped
+    for (int k = lane; k < L; k += 32) {
+        float2 xk = y[k];
+        float2 xl = y[L - k];
+        if (k == 0) {
+            xk.y = 0.f;
+            xl.y = 0.f;
+        }
+        const float2 xc = cconj(xl);
+        const float2 e = cadd(xk, xc);
+        const float2 o = cmul(csub(xk, xc), cconj(tw[k]));
+        const float2 zz = cadd(e, cmul_pi(o));
+        z[k] = cconj(zz);  // inverse via conj trick
+    }
+    __syncwarp();
+    fft_warp<L, 2>(z, tw, lane);
+    const float inv = 1.0f / ((float)N * (float)N);
+    float* out = phase + (size_t)row * N;
+    for (int m = lane; m < L; m += 32) {
+        const float2 v = cconj(z[m]);
+        out[2 * m] = atan2f(v.x * inv, a);
+        out[2 * m + 1] = atan2f(v.y * inv, a);
+    }
+}
+
+template <int N>
+static cudaError_t phase_n(const float2* O, const int32_t* Nn, const double* dcpart, int nsplit,
+                           int n_bf, float2* Y, const float2* tw, float* phase, cudaStream_t st) {
+    constexpr int CW = (N / 2 >= 16) ? 16 : N / 2;
+    constexpr int NG = (N / 2) / CW;
+    const size_t cs = (size_t)N * sizeof(float2) + (size_t)(CW + 1) * (N + 1) * sizeof(float2);
+    const size_t rs = (size_t)N * sizeof(float2) + (size_t)(kPhaseThreads / 32) * (N / 2) * sizeof(float2);
+    cudaError_t e;
+    if ((e = cudaFuncSetAttribute(c2r_cols_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)cs)) != cudaSuccess)
+        return e;
+    c2r_cols_kernel<N><<<NG, kPhaseThreads, cs, st>>>(O, Nn, Y, tw);
+    count_launch();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    constexpr int RPB = kPhaseThreads / 32;
+    c2r_rows_kernel<N><<<(N + RPB - 1) / RPB, kPhaseThreads, rs, st>>>(Y, dcpart, nsplit, n_bf, tw, phase);
+    count_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_phase(const float2* O, const int32_t* Nn, const double* dcpart, int nsplit, int n_bf,
+                         int n, float2* Y, const float2* tw, float* phase, cudaStream_t st) {
+    switch (n) {
+        case 8: return phase_n<8>(O, Nn, dcpart, nsplit, n_bf, Y, tw, phase, st);
+        case 16: return phase_n<16>(O, Nn, dcpart, nsplit, n_bf, Y, tw, phase, st);
+        case 32: return phase_n<32>(O, Nn, dcpart, nsplit, n_bf, Y, tw, phase, st);
+        case 64: return phase_n<64>(O, Nn, dcpart, nsplit, n_bf, Y, tw, phase, st);
+        case 128: return phase_n<128>(O, Nn, dcpart, nsplit, n_bf, Y, tw, phase, st);
+        case 256: return phase_n<256>(O, Nn, dcpart, nsplit, n_bf, Y, tw, phase, st);
+        case 512: return phase_n<512>(O, Nn, dcpart, nsplit, n_bf, Y, tw, phase, st);
+        case 1024: return phase_n<1024>(O, Nn, dcpart, nsplit, n_bf, Y, tw, phase, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// score_s = sum_q |O_s(q)|^2 / sum_q N_s(q), one block per set, float64 sums
+// ---------------------------------------------------------------------------
+__global__ void score_kernel(const float2* __restrict__ O, const int32_t* __restrict__ Nn, int nq,
+                             double* __restrict__ score) {
+    __shared__ double s_num[256];
+    __shared__ long long s_den[256];
+    const int s = blockIdx.x;
+    double num = 0.0;
+    long long den = 0;
+    for (int q = threadIdx.x; q < nq; q += 256) {
+        const float2 o = O[(size_t)s * nq + q];
+        num += (double)o.x * (double)o.x + (double)o.y * (double)o.y;
+        den += Nn[(size_t)s * nq + q];
+    }
+    s_num[threadIdx.x] = num;
+    s_den[threadIdx.x] = den;
+    __syncthreads();
+    for (int w = 128; w > 0; w >>= 1) {
+        if (threadIdx.x < w) {
+            s_num[threadIdx.x] += s_num[threadIdx.x + w];
+            s_den[threadIdx.x] += s_den[threadIdx.x + w];
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) score[s] = s_den[0] > 0 ? s_num[0] / (double)s_den[0] : 0.0;
+}
+
+cudaError_t launch_score(const float2* O, const int32_t* Nn, int B, int nq, double* score,
+                         cudaStream_t st) {
+    score_kernel<<<B, 256, 0, st>>>(O, Nn, nq, score);
+    count_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace ssb

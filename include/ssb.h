@@ -1,0 +1,188 @@
+/*
+ * ssb.h -- C ABI of the GB300 single-sideband (SSB) direct-ptychography library.
+ *
+ * The library computes, on one GPU, the data-parallel hot path of
+ * aberration-corrected SSB ptychography from 4D-STEM frames:
+ *
+ *   1. G(q,k): gather the bright-field (BF) detector pixels from raw
+ *      (scan_y, scan_x, det_y, det_x) frames and take the 2D real-to-complex
+ *      FFT over the two scan axes for every BF pixel, stored as the Hermitian
+ *      half plane (n, n/2+1).  Source: quantem.gpu "Historical WebGPU G(q,k)
+ *      memory experiment", sections "Why herm is exactly lossless" and
+ *      "Implementation" (G is the scan-space FFT of real intensity traces, so
+ *      G(-q,k) = conj G(q,k) and the half plane is lossless).
+ *   2. Per scan frequency q, the trotter-masked, aberration-phase-weighted sum
+ *      over BF pixels k, for one or B <= 8 aberration sets per pass.  Source:
+ *      quantem.gpu "Tilt-corrected SSB on CUDA: fit and preview speed",
+ *      sections "Where the time went" and "Changes" (per (k, q, set): chi,
+ *      aperture tests, sincos; per-set accumulators unrolled to a compile-time
+ *      maximum).
+ *   3. The object estimate: the corrected half-plane spectrum is summed over k,
+ *      normalised, and brought back to real space by one complex-to-real
+ *      inverse FFT plus atan2.  Source: "Historical WebGPU G(q,k) memory
+ *      experiment", section "Object-redraw fast path" (mean over BF in Fourier
+ *      space, then one inverse 2D FFT and one atan2); "Tilt-corrected SSB on
+ *      CUDA", section "Open" (the corrected spectrum is anti-Hermitian except
+ *      at DC, so a half-plane complex-to-real transform suffices).
+ *
+ * Conventions (the plainest reading of the pages; all fixed here):
+ *   - Detector pixel (i, j) has k = ((j - det_center_x) Dk, (i - det_center_y) Dk),
+ *     Dk = det_pitch_invA, detector rotation 0.
+ *   - Half-plane entry (row, col), row in [0, n), col in [0, n/2], is the scan
+ *     frequency q = (f_x, f_y) dq with f_x = col, f_y = row for row < n/2 and
+ *     row - n otherwise, dq = 1 / (n scan_step_A).
+ *   - Aperture of a set: A(v) = 1 iff |v - k_t|^2 <= (alpha/lambda)^2, with
+ *     k_t = (tilt_x, tilt_y)/lambda.  Evaluated as the float32 sequence
+ *     dx = px - tx; dy = py - ty; d2 = dx*dx + dy*dy; d2 <= r2, every step a
+ *     separately rounded IEEE float32 operation (no fused multiply-add), with
+ *     px, py = float32(k) -/+ float32(q), tx, ty = float32(k_t) and
+ *     r2 = float32((alpha/lambda)^2).  Integer outcomes (trotter membership,
+ *     N(q)) are therefore reproducible bit for bit.
+ *   - Trotters: a = A(k), m = A(k - q), p = A(k + q); T- = a & m & !p,
+ *     T+ = a & p & !m.  On T- the weight is exp(-i (chi(k) - chi(k - q))), on
+ *     T+ it is -exp(+i (chi(k) - chi(k + q))); chi is the Krivanek aberration
+ *     function of v - k_t (12 a/b coefficients through 4th order, Angstrom).
+ *     O(q) = sum_k G(q,k) w(q,k), N(q) = |T-(q)| + |T+(q)|.
+ *   - Phase image: S(q) = O(q)/N(q) (0 where N = 0), zeroed on the Nyquist row
+ *     f_y = -n/2 and column f_x = n/2 and at DC; b = irfft2(-i S) with numpy
+ *     semantics (1/n^2 normalisation, imaginary parts of self-conjugate bins
+ *     dropped); a = mean_k G(0,k) / n^2; phase = atan2(b, a).
+ *   - Score of a set over a band list: sum_q |O(q)|^2 / sum_q N(q).
+ *
+ * Ownership and asynchrony: every device buffer is owned by the caller.  The
+ * library never allocates or frees memory; kernels that need scratch space use
+ * the caller's workspace, sized by ssb_workspace_bytes().  Device calls are
+ * asynchronous on the given stream (a cudaStream_t passed as void*; NULL is the
+ * legacy default stream) and never synchronise the host.
+ *
+ * Errors: every entry point returns an ssb_status.  Argument checks happen on
+ * the host before anything is launched; on SSB_CUDA_ERROR the launch error
+ * text is available from ssb_last_error() (thread-local).  Checks cover null
+ * pointers, sizes and workspace size; the contents of device buffers
+ * (bf_idx_dev, band_dev) are the caller's responsibility: every index must be
+ * in range (detector indices < det_y*det_x, band entries < n*(n/2+1)).
+ */
+#ifndef SSB_H
+#define SSB_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Scan and detector geometry.  The scan is n x n (n a power of two, 8..1024). */
+typedef struct ssb_geometry {
+    int n;
+    int det_y, det_x;
+    double scan_step_A;      /* Delta: scan step (Angstrom)                   */
+    double det_pitch_invA;   /* Dk: detector pixel pitch (1/Angstrom)         */
+    double wavelength_A;     /* lambda (Angstrom)                             */
+    double semiangle_rad;    /* alpha: probe-forming aperture semi-angle      */
+    double det_center_y;     /* detector pixel coordinate of k_y = 0          */
+    double det_center_x;     /* detector pixel coordinate of k_x = 0          */
+} ssb_geometry;
+
+/* One aberration set: Krivanek a/b coefficients (Angstrom) and probe tilt. */
+typedef struct ssb_aberr {
+    double C10, C12a, C12b, C21a, C21b, C23a, C23b, C30, C32a, C32b, C34a, C34b;
+    double tilt_x_rad, tilt_y_rad;
+} ssb_aberr;
+
+typedef enum ssb_dtype { SSB_U16 = 0, SSB_F32 = 1 } ssb_dtype;
+
+typedef enum ssb_status {
+    SSB_OK = 0,
+    SSB_INVALID_ARG = 1,          /* null pointer, non-positive size, bad dtype/op     */
+    SSB_UNSUPPORTED = 2,          /* n not a power of two in [8, 1024], B not in 1..8  */
+    SSB_WORKSPACE_TOO_SMALL = 3,  /* ws_bytes < ssb_workspace_bytes(...)               */
+    SSB_CUDA_ERROR = 4            /* a launch failed; see ssb_last_error()             */
+} ssb_status;
+
+typedef enum ssb_op { SSB_OP_BUILD = 0, SSB_OP_RECON = 1, SSB_OP_SCORE = 2 } ssb_op;
+
+#define SSB_MAX_SETS 8
+#define SSB_MIN_N 8
+#define SSB_MAX_N 1024
+
+/*
+ * Bright-field pixel set (host only, no GPU).  Pixels (i, j) with
+ *   ((j - cx) Dk - tx/lambda)^2 + ((i - cy) Dk - ty/lambda)^2 <= (alpha/lambda)^2
+ * evaluated in float64 in exactly that order (no fused multiply-add), tilt from
+ * `base`.  Output: row-major detector indices i*det_x + j, ascending.
+ * `out` (host, may be NULL) must hold det_y*det_x entries; *n_bf receives the
+ * count.  Source: "Historical WebGPU G(q,k) memory experiment", section
+ * "Gotchas recorded" (only aperture-active BF pixels carry G).
+ */
+int ssb_bf_indices(const ssb_geometry* geom, const ssb_aberr* base,
+                   int32_t* out, int* n_bf);
+
+/*
+ * Band list (host only).  Half-plane entries row*(n/2+1)+col with
+ * (qmin/dq)^2 <= f_y^2 + f_x^2 <= (qmax/dq)^2, bounds in float64, ascending.
+ * `out` (host, may be NULL) must hold n*(n/2+1) entries; *nq receives the
+ * count.  Source: "Tilt-corrected SSB on CUDA", section "Setup" (fit band
+ * 0.2 to 0.9 1/A, 44,247 frequencies on a 512^2 scan).
+ */
+int ssb_band_indices(const ssb_geometry* geom, double qmin, double qmax,
+                     int32_t* out, int* nq);
+
+/*
+ * Bytes of device workspace an operation needs (0 on invalid arguments).
+ * op = SSB_OP_BUILD, SSB_OP_RECON (B ignored, nq ignored) or SSB_OP_SCORE
+ * (B sets over nq band entries).  The workspace must be 256-byte aligned.
+ */
+size_t ssb_workspace_bytes(const ssb_geometry* geom, int n_bf, int op, int B, int nq);
+
+/*
+ * G(q,k) build.  frames: device, (n, n, det_y, det_x) uint16 or float32,
+ * contiguous.  bf_idx_dev: device int32[n_bf] detector indices.  G_dev:
+ * device complex64 [n_bf][n][n/2+1] (q_x fastest), fully overwritten.
+ * G(q,k) = sum_r x_k(r) exp(-2 pi i (f_y r_y + f_x r_x)/n), float32 arithmetic.
+ * Source: "Historical WebGPU G(q,k) memory experiment", sections
+ * "Implementation" and "Memory planning table" (layout and size
+ * n_bf * n * (n/2+1) * 8 bytes).
+ */
+int ssb_build_G(const void* frames, int dtype, const ssb_geometry* geom,
+                const int32_t* bf_idx_dev, int n_bf, void* G_dev,
+                void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * One reconstruction at one aberration set (set: host pointer).
+ * Writes O_dev (complex64 [n][n/2+1]), N_dev (int32 [n][n/2+1]) and phase_dev
+ * (float32 [n][n], row = scan_y).  Source: "Historical WebGPU G(q,k) memory
+ * experiment", section "Object-redraw fast path"; "Tilt-corrected SSB on
+ * CUDA", sections "Changes" and "Open".
+ */
+int ssb_reconstruct(const void* G_dev, const ssb_geometry* geom,
+                    const int32_t* bf_idx_dev, int n_bf, const ssb_aberr* set,
+                    void* O_dev, int32_t* N_dev, float* phase_dev,
+                    void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Batched scoring of B aberration sets (sets: host array of B) over a band
+ * list (band_dev: device int32[nq] half-plane entries).  Writes O_dev
+ * (complex64 [B][nq]), N_dev (int32 [B][nq]) and score_dev (float64 [B]).
+ * Set s of a B-set call equals the corresponding single-set call bit for bit.
+ * Source: "Tilt-corrected SSB on CUDA", sections "Where the time went" and
+ * "Changes" (eight sets per pass, per-set loops unrolled to a compile-time
+ * maximum with a uniform b < B guard).
+ */
+int ssb_score_batch(const void* G_dev, const ssb_geometry* geom,
+                    const int32_t* bf_idx_dev, int n_bf, const ssb_aberr* sets, int B,
+                    const int32_t* band_dev, int nq,
+                    void* O_dev, int32_t* N_dev, double* score_dev,
+                    void* ws, size_t ws_bytes, void* stream);
+
+/* Text of the last error on this host thread ("" if none). */
+const char* ssb_last_error(void);
+
+/* Number of kernels this library has launched in this process. */
+long long ssb_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSB_H */

@@ -1,0 +1,163 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol the
+header declares, computes the host-side index sets bit for bit like the
+oracle, and rejects bad arguments with status codes before launching."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import electron_microscopy_gb300 as ssb
+from oracle import ssb_oracle as O
+from synth import configs as C
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(ssb.LIB_PATH):
+        import __graft_entry__ as ge
+        ge.build()
+    return ssb.load()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "ssb.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ssb_[A-Za-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_names():
+    assert set(_declared_functions()) == set(ssb.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", ssb.LIB_PATH], capture_output=True, text=True).stdout
+    syms = set(line.split()[-1] for line in out.splitlines() if line.strip())
+    for fn in _declared_functions():
+        assert fn in syms, fn
+        assert hasattr(lib, fn)
+
+
+@pytest.mark.parametrize("name", ["tiny", "small", "full", "large"])
+@pytest.mark.parametrize("tilt", [(0.0, 0.0), (5.92e-3, -0.07e-3), (-3.3e-3, 7.1e-3)])
+def test_bf_indices_match_oracle(lib, name, tilt):
+    g = C.geometry(C.WORKLOADS[name])
+    ab = C.Aberrations(tilt_x_rad=tilt[0], tilt_y_rad=tilt[1])
+    got = ssb.bf_indices(g, ab)
+    ref = O.bf_indices(g, *tilt)
+    assert np.array_equal(got, ref)
+
+
+def test_bf_indices_on_exact_edge(lib):
+    # a geometry whose disk edge falls exactly on pixel centres
+    g = C.Geometry(n=8, det_y=11, det_x=11, scan_step_A=1.0, det_pitch_invA=0.5,
+                   wavelength_A=0.02, semiangle_rad=0.05, det_center_y=5.0, det_center_x=5.0)
+    got = ssb.bf_indices(g, C.Aberrations())
+    ref = O.bf_indices(g)
+    assert np.array_equal(got, ref)
+    assert len(ref) == 81  # radius 2.5 1/A = 5 px: the 4 axis pixels at distance 5 are in
+
+
+@pytest.mark.parametrize("n", [8, 32, 128, 512, 1024])
+def test_band_indices_match_oracle(lib, n):
+    g = C.Geometry(n=n, det_y=8, det_x=8, scan_step_A=0.373, det_pitch_invA=0.1,
+                   wavelength_A=0.019687, semiangle_rad=0.03, det_center_y=4, det_center_x=4)
+    for lo, hi in [(0.2, 0.9), (0.0, 0.5), (0.0, 10.0), (1.0, 1.0)]:
+        got = ssb.band_indices(g, lo, hi)
+        ref = O.band_indices(g, lo, hi)
+        assert np.array_equal(got, ref)
+
+
+def test_band_count_printed_on_pages(lib):
+    g = C.geometry(C.WORKLOADS["full"])
+    assert len(ssb.band_indices(g, 0.2, 0.9)) == 44247
+
+
+def test_workspace_bytes(lib):
+    g = C.geometry(C.WORKLOADS["full"])
+    assert ssb.workspace_bytes(g, 9354, ssb.OP_BUILD) > 0
+    r = ssb.workspace_bytes(g, 9354, ssb.OP_RECON)
+    assert r >= 512 * 257 * (8 + 4)
+    s1 = ssb.workspace_bytes(g, 9354, ssb.OP_SCORE, 1, 44247)
+    s8 = ssb.workspace_bytes(g, 9354, ssb.OP_SCORE, 8, 44247)
+    assert 0 < s1 < s8
+    assert ssb.workspace_bytes(g, 9354, ssb.OP_SCORE, 9, 44247) == 0
+    assert ssb.workspace_bytes(g, 0, ssb.OP_RECON) == 0
+    assert ssb.workspace_bytes(g, 10, 7) == 0
+    bad = C.Geometry(**{**g.__dict__, "n": 100})
+    assert ssb.workspace_bytes(bad, 10, ssb.OP_RECON) == 0
+
+
+def _g(**kw):
+    g = C.geometry(C.WORKLOADS["tiny"])
+    return ssb.to_geometry(C.Geometry(**{**g.__dict__, **kw}))
+
+
+FAKE = ctypes.c_void_p(1 << 20)  # never dereferenced: every call below fails its host checks
+
+
+def _err(lib):
+    return lib.ssb_last_error().decode()
+
+
+def test_error_codes_build(lib):
+    g = _g()
+    big = 1 << 30
+    rc = lib.ssb_build_G(None, 0, ctypes.byref(g), FAKE, 10, FAKE, FAKE, big, None)
+    assert rc == ssb.SSB_INVALID_ARG and "NULL" in _err(lib)
+    rc = lib.ssb_build_G(FAKE, 7, ctypes.byref(g), FAKE, 10, FAKE, FAKE, big, None)
+    assert rc == ssb.SSB_INVALID_ARG
+    for n in (100, 4, 2048, 0, -8):
+        rc = lib.ssb_build_G(FAKE, 0, ctypes.byref(_g(n=n)), FAKE, 10, FAKE, FAKE, big, None)
+        assert rc == ssb.SSB_UNSUPPORTED, n
+    rc = lib.ssb_build_G(FAKE, 0, ctypes.byref(_g(det_x=0)), FAKE, 10, FAKE, FAKE, big, None)
+    assert rc == ssb.SSB_INVALID_ARG
+    rc = lib.ssb_build_G(FAKE, 0, ctypes.byref(g), FAKE, 0, FAKE, FAKE, big, None)
+    assert rc == ssb.SSB_INVALID_ARG
+    rc = lib.ssb_build_G(FAKE, 0, ctypes.byref(g), FAKE, 24 * 24 + 1, FAKE, FAKE, big, None)
+    assert rc == ssb.SSB_INVALID_ARG
+    rc = lib.ssb_build_G(FAKE, 0, ctypes.byref(g), FAKE, 10, FAKE, FAKE, 16, None)
+    assert rc == ssb.SSB_WORKSPACE_TOO_SMALL and "needs" in _err(lib)
+    rc = lib.ssb_build_G(FAKE, 0, ctypes.byref(g), FAKE, 10, FAKE, ctypes.c_void_p((1 << 20) + 8), big, None)
+    assert rc == ssb.SSB_INVALID_ARG and "aligned" in _err(lib)
+    rc = lib.ssb_build_G(FAKE, 0, ctypes.byref(_g(wavelength_A=0.0)), FAKE, 10, FAKE, FAKE, big, None)
+    assert rc == ssb.SSB_INVALID_ARG
+    rc = lib.ssb_build_G(FAKE, 0, None, FAKE, 10, FAKE, FAKE, big, None)
+    assert rc == ssb.SSB_INVALID_ARG
+
+
+def test_error_codes_reconstruct_and_score(lib):
+    g = _g()
+    a = ssb.Aberr()
+    big = 1 << 30
+    rc = lib.ssb_reconstruct(FAKE, ctypes.byref(g), FAKE, 10, None, FAKE, FAKE, FAKE, FAKE, big, None)
+    assert rc == ssb.SSB_INVALID_ARG
+    rc = lib.ssb_reconstruct(FAKE, ctypes.byref(g), FAKE, 10, ctypes.byref(a), FAKE, FAKE, FAKE, FAKE, 100, None)
+    assert rc == ssb.SSB_WORKSPACE_TOO_SMALL
+    nan = ssb.Aberr(C10=float("nan"))
+    rc = lib.ssb_reconstruct(FAKE, ctypes.byref(g), FAKE, 10, ctypes.byref(nan), FAKE, FAKE, FAKE, FAKE, big, None)
+    assert rc == ssb.SSB_INVALID_ARG
+    sets = (ssb.Aberr * 9)()
+    for B in (0, 9):
+        rc = lib.ssb_score_batch(FAKE, ctypes.byref(g), FAKE, 10, sets, B, FAKE, 5, FAKE, FAKE, FAKE, FAKE, big, None)
+        assert rc == ssb.SSB_UNSUPPORTED, B
+    rc = lib.ssb_score_batch(FAKE, ctypes.byref(g), FAKE, 10, sets, 2, FAKE, 0, FAKE, FAKE, FAKE, FAKE, big, None)
+    assert rc == ssb.SSB_INVALID_ARG
+    rc = lib.ssb_score_batch(FAKE, ctypes.byref(g), FAKE, 10, sets, 2, FAKE, 32 * 17 + 1, FAKE, FAKE, FAKE, FAKE,
+                             big, None)
+    assert rc == ssb.SSB_INVALID_ARG
+    rc = lib.ssb_score_batch(FAKE, ctypes.byref(g), FAKE, 10, sets, 2, None, 5, FAKE, FAKE, FAKE, FAKE, big, None)
+    assert rc == ssb.SSB_INVALID_ARG
+    rc = lib.ssb_score_batch(FAKE, ctypes.byref(g), FAKE, 10, sets, 2, FAKE, 5, FAKE, FAKE, FAKE, FAKE, 64, None)
+    assert rc == ssb.SSB_WORKSPACE_TOO_SMALL
+
+
+def test_no_launches_from_failed_checks(lib):
+    before = lib.ssb_launch_count()
+    g = _g(n=100)
+    lib.ssb_build_G(FAKE, 0, ctypes.byref(g), FAKE, 10, FAKE, FAKE, 1 << 30, None)
+    assert lib.ssb_launch_count() == before

@@ -1,0 +1,145 @@
+"""Parity at the full workload size (512^2 scan, 192^2 uint16 detector,
+~9.35k BF pixels) in the launch configuration the benchmark times.
+
+The oracle cannot rebuild all of G or O here in seconds, so it checks sampled
+outputs it computes one by one from the same frames: whole G planes of a few
+BF pixels, O(q) and N(q) at a few q (G(q, .) by a direct DFT over all scan
+positions), N(q) at a few thousand q, and the batched scores' O/N over the
+band at sampled entries.  The phase image stage runs in the same launch
+geometry as the n = 512 case of test_gpu_parity (checked element by element
+there); here it is checked for finiteness and recovery of the ground truth.
+"""
+import numpy as np
+import pytest
+
+from oracle import ssb_oracle as O
+from synth import configs as C
+from synth import forward as F
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+torch = pytest.importorskip("torch")
+
+TOL = 1e-4
+
+
+def rel(a, b):
+    return float(np.linalg.norm(np.ravel(a - b)) / np.linalg.norm(np.ravel(b)))
+
+
+@pytest.fixture(scope="module")
+def full(request):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__ as ge
+    ge.build()
+    import electron_microscopy_gb300 as ssb
+    d = F.make_torch_dataset("full", device="cuda")
+    geom, ab = d["geom"], d["ab"]
+    bf = ssb.bf_indices(geom, ab)
+    bfd = torch.from_numpy(bf).cuda()
+    G = ssb.build_G(d["frames"], geom, bfd)
+    Od, Nd, ph = ssb.reconstruct(G, geom, bfd, ab)
+    torch.cuda.synchronize()
+    # host copy of the BF columns only, (n*n, N_bf) uint16
+    n = geom.n
+    cols = d["frames"].view(n * n, -1).index_select(1, bfd.long()).cpu().numpy().view(np.uint16)
+    yield {"ssb": ssb, "d": d, "geom": geom, "ab": ab, "bf": bf, "bfd": bfd, "G": G, "O": Od,
+           "N": Nd, "phase": ph, "cols": cols}
+    del G
+
+
+def test_bf_count_and_counts(full):
+    assert 9300 <= len(full["bf"]) <= 9400
+    assert 10 <= full["d"]["max_count"] <= 40
+
+
+def test_sampled_G_planes(full):
+    n = full["geom"].n
+    cols = full["cols"]
+    for b in (0, 1, 777, len(full["bf"]) // 2, len(full["bf"]) - 1):
+        x = cols[:, b].astype(np.float64).reshape(n, n)
+        ref = np.fft.rfft2(x)
+        got = full["G"][b].cpu().numpy()
+        assert rel(got, ref) < TOL, b
+
+
+def _direct_G_at(cols, n, fys, fxs):
+    """G(q, k) for a few q by a direct DFT over all n*n scan positions."""
+    ry, rx = np.divmod(np.arange(n * n), n)
+    out = np.zeros((len(fys), cols.shape[1]), dtype=np.complex128)
+    step = 16384
+    for s in range(0, n * n, step):
+        X = cols[s:s + step].astype(np.float64)
+        ang = -2.0 * np.pi * (np.outer(fys, ry[s:s + step]) + np.outer(fxs, rx[s:s + step])) / n
+        out += np.cos(ang) @ X + 1j * (np.sin(ang) @ X)
+    return out
+
+
+def test_sampled_O_and_N(full):
+    g, ab, bf = full["geom"], full["ab"], full["bf"]
+    n, h = g.n, g.n // 2 + 1
+    fys = np.array([3, -40, 100, -150, 7, 200, -255])
+    fxs = np.array([5, 0, 60, 120, 200, 31, 17])
+    Gq = _direct_G_at(full["cols"], n, fys, fxs)          # (Q, N_bf)
+    dq = 1.0 / (n * g.scan_step_A)
+    tm, tp = O.trotters(g, ab, bf, fxs * dq, fys * dq)
+    w = O.weights(g, ab, bf, fxs * dq, fys * dq, tm, tp)
+    Oref = (Gq * w).sum(axis=1)
+    Nref = (tm | tp).sum(axis=1)
+    rows = fys % n
+    Od = full["O"].cpu().numpy()
+    Nd = full["N"].cpu().numpy()
+    for i in range(len(fys)):
+        assert Nd[rows[i], fxs[i]] == Nref[i]
+        if Nref[i] > 0:
+            assert abs(Od[rows[i], fxs[i]] - Oref[i]) <= TOL * abs(Oref[i]) + 1e-3, i
+
+
+def test_N_bitexact_on_many_q(full):
+    g, ab, bf = full["geom"], full["ab"], full["bf"]
+    n, h = g.n, g.n // 2 + 1
+    rng = np.random.default_rng(0)
+    entries = rng.choice(n * h, size=3000, replace=False)
+    qx_col, qy_row = O.q_coords(g)
+    tm, tp = O.trotters(g, ab, bf, qx_col[entries % h], qy_row[entries // h])
+    Nref = (tm | tp).sum(axis=1)
+    Nd = full["N"].cpu().numpy().ravel()[entries]
+    assert np.array_equal(Nd, Nref)
+
+
+def test_phase_image_recovers_truth(full):
+    ph = full["phase"].cpu().numpy()
+    assert np.all(np.isfinite(ph))
+    r = np.corrcoef(ph.ravel(), full["d"]["truth"].ravel())[0, 1]
+    assert r > 0.5
+
+
+def test_batched_scores_sampled(full):
+    ssb = full["ssb"]
+    g, bf, bfd = full["geom"], full["bf"], full["bfd"]
+    n, h = g.n, g.n // 2 + 1
+    band = ssb.band_indices(g, 0.2, 0.9)
+    assert len(band) == 44247
+    sets = C.perturbed_sets(full["ab"], 8, seed=4)
+    Ob, Nb, sc = ssb.score_batch(full["G"], g, bfd, sets, torch.from_numpy(band).cuda())
+    torch.cuda.synchronize()
+    pick = band[np.array([0, 5000, 20000, 44246])]
+    fys = np.where(pick // h < n // 2, pick // h, pick // h - n)
+    fxs = pick % h
+    Gq = _direct_G_at(full["cols"], n, fys, fxs)
+    dq = 1.0 / (n * g.scan_step_A)
+    pos = np.searchsorted(band, pick)
+    for s, ab in enumerate(sets):
+        tm, tp = O.trotters(g, ab, bf, fxs * dq, fys * dq)
+        w = O.weights(g, ab, bf, fxs * dq, fys * dq, tm, tp)
+        Oref = (Gq * w).sum(axis=1)
+        Nref = (tm | tp).sum(axis=1)
+        assert np.array_equal(Nb[s].cpu().numpy()[pos], Nref)
+        got = Ob[s].cpu().numpy()[pos]
+        assert np.all(np.abs(got - Oref) <= TOL * np.abs(Oref) + 1e-3)
+    # the score is sum |O|^2 / sum N over the stored band values
+    Oh = Ob.cpu().numpy().astype(np.complex128)
+    Nh = Nb.cpu().numpy()
+    for s in range(8):
+        ref = np.sum(np.abs(Oh[s]) ** 2) / np.sum(Nh[s])
+        assert abs(sc[s].item() - ref) <= 1e-9 * ref

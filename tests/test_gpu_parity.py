@@ -1,0 +1,226 @@
+"""GPU parity: the CUDA library (called through its C ABI) against the CPU
+oracle on the same seeded inputs.
+
+Bars: bit-exact for integer work (trotter counts N, BF and band index sets);
+relative L2 <= 1e-4 for the float32 paths (G, O, phase, score), the tolerance
+stated for the hot path's float32 results.
+"""
+import numpy as np
+import pytest
+
+from oracle import ssb_oracle as O
+from synth import configs as C
+from synth import forward as F
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-4
+
+torch = pytest.importorskip("torch")
+
+
+def rel(a, b):
+    a = np.asarray(a)
+    b = np.asarray(b)
+    den = np.linalg.norm(b.ravel())
+    return float(np.linalg.norm((a - b).ravel()) / (den if den > 0 else 1.0))
+
+
+@pytest.fixture(scope="module")
+def ssb():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__ as ge
+    ge.build()
+    import electron_microscopy_gb300 as m
+    return m
+
+
+def _dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+def _frames_dev(frames):
+    if frames.dtype == np.uint16:
+        return _dev(frames.view(np.int16))
+    return _dev(frames)
+
+
+def _run_all(ssb, frames, geom, ab, bf):
+    fd = _frames_dev(frames)
+    bfd = _dev(bf)
+    G = ssb.build_G(fd, geom, bfd)
+    Od, Nd, ph = ssb.reconstruct(G, geom, bfd, ab)
+    torch.cuda.synchronize()
+    return G.cpu().numpy(), Od.cpu().numpy(), Nd.cpu().numpy(), ph.cpu().numpy()
+
+
+def _check_against_oracle(ssb, frames, geom, ab, tol=TOL):
+    bf = O.bf_indices(geom, ab.tilt_x_rad, ab.tilt_y_rad)
+    assert np.array_equal(ssb.bf_indices(geom, ab), bf)
+    G, Od, Nd, ph = _run_all(ssb, frames, geom, ab, bf)
+    ref = O.reconstruct(frames, geom, ab, bf_idx=bf)
+    n, h = geom.n, geom.n // 2 + 1
+    assert G.shape == (len(bf), n, h)
+    assert rel(G, ref["G"]) < tol
+    assert np.array_equal(Nd.ravel(), ref["N"])
+    assert rel(Od.ravel(), ref["O"]) < tol
+    assert rel(ph, ref["phase"]) < tol
+    return G, Od, Nd, ph, ref
+
+
+# ----------------------------------------------------------------------------
+# the seeded workloads
+# ----------------------------------------------------------------------------
+
+def test_tiny_workload(ssb, tiny_dataset):
+    d = tiny_dataset
+    _, _, _, ph, ref = _check_against_oracle(ssb, d["frames"], d["geom"], d["ab"])
+    # the recovered phase tracks the ground truth like the oracle's does
+    r = np.corrcoef(ph.ravel(), d["truth"].ravel())[0, 1]
+    assert r > 0.95
+
+
+def test_small_workload(ssb, small_dataset):
+    d = small_dataset
+    _check_against_oracle(ssb, d["frames"], d["geom"], d["ab"])
+
+
+# ----------------------------------------------------------------------------
+# sizes, ragged tails and edge cases on random counts
+# ----------------------------------------------------------------------------
+
+def _geom(n, det, dk, step=C.SCAN_STEP_A):
+    return C.Geometry(n=n, det_y=det, det_x=det, scan_step_A=step, det_pitch_invA=dk,
+                      wavelength_A=C.WAVELENGTH_300KV_A, semiangle_rad=C.SEMIANGLE_RAD,
+                      det_center_y=det // 2, det_center_x=det // 2)
+
+
+AB = C.Aberrations(C10=-60.0, C12a=12.0, C12b=-20.0, C21a=15.0, C21b=-9.0, C23a=20.0, C23b=5.0,
+                   C30=4e3, C32a=-3e3, C32b=2e3, C34a=1e3, C34b=-2.5e3, tilt_x_rad=2e-3, tilt_y_rad=-1e-3)
+
+
+@pytest.mark.parametrize("n,det,dk", [(8, 6, 0.6), (16, 10, 0.35), (64, 14, 0.25), (256, 10, 0.4)])
+def test_random_counts_sizes(ssb, n, det, dk):
+    rng = np.random.default_rng(n)
+    frames = rng.poisson(3.0, size=(n, n, det, det)).astype(np.uint16)
+    _check_against_oracle(ssb, frames, _geom(n, det, dk), AB)
+
+
+def test_float32_frames_ragged(ssb):
+    # n_bf = 45: one full 32-pixel group plus a ragged tail
+    rng = np.random.default_rng(7)
+    n, det = 32, 9
+    frames = rng.uniform(0, 10, size=(n, n, det, det)).astype(np.float32)
+    g = _geom(n, det, 0.45)
+    bf = O.bf_indices(g, AB.tilt_x_rad, AB.tilt_y_rad)
+    assert len(bf) % 32 != 0
+    _check_against_oracle(ssb, frames, g, AB)
+
+
+def test_single_bf_pixel(ssb):
+    rng = np.random.default_rng(8)
+    n = 32
+    g = C.Geometry(n=n, det_y=3, det_x=3, scan_step_A=C.SCAN_STEP_A, det_pitch_invA=2.0,
+                   wavelength_A=C.WAVELENGTH_300KV_A, semiangle_rad=C.SEMIANGLE_RAD,
+                   det_center_y=1, det_center_x=1)
+    bf = O.bf_indices(g)
+    assert len(bf) == 1
+    frames = rng.poisson(5.0, size=(n, n, 3, 3)).astype(np.uint16)
+    _check_against_oracle(ssb, frames, g, C.Aberrations(C10=30.0))
+
+
+def test_full_scan_size_small_detector(ssb):
+    """n = 512 (the full workload's FFT and image launch geometry) with a
+    12 x 12 detector so the oracle finishes in seconds."""
+    rng = np.random.default_rng(9)
+    n, det = 512, 12
+    frames = rng.poisson(3.0, size=(n, n, det, det)).astype(np.uint16)
+    g = _geom(n, det, 0.33)
+    _check_against_oracle(ssb, frames, g, AB)
+
+
+def test_max_scan_size_1024(ssb):
+    rng = np.random.default_rng(10)
+    n, det = 1024, 6
+    frames = rng.poisson(3.0, size=(n, n, det, det)).astype(np.uint16)
+    g = _geom(n, det, 0.6)
+    _check_against_oracle(ssb, frames, g, AB.replace(tilt_x_rad=0.0, tilt_y_rad=0.0))
+
+
+def test_zero_frames_give_zero_G_and_flat_phase(ssb):
+    n, det = 16, 8
+    frames = np.zeros((n, n, det, det), dtype=np.uint16)
+    frames[..., :, :] = 4
+    g = _geom(n, det, 0.4)
+    bf = O.bf_indices(g)
+    G, Od, Nd, ph = _run_all(ssb, frames, g, C.Aberrations(), bf)
+    assert np.allclose(G[:, 0, 0], 4.0 * n * n)
+    G2 = G.copy()
+    G2[:, 0, 0] = 0
+    assert np.abs(G2).max() < 1e-3
+    assert np.abs(ph).max() < 1e-6
+
+
+# ----------------------------------------------------------------------------
+# batched scoring
+# ----------------------------------------------------------------------------
+
+@pytest.fixture(scope="module")
+def small_G(ssb, small_dataset):
+    d = small_dataset
+    bf = O.bf_indices(d["geom"], d["ab"].tilt_x_rad, d["ab"].tilt_y_rad)
+    G = ssb.build_G(_frames_dev(d["frames"]), d["geom"], _dev(bf))
+    return d, bf, G
+
+
+def test_score_batch_matches_oracle(ssb, small_G):
+    d, bf, G = small_G
+    g = d["geom"]
+    band = O.band_indices(g, 0.2, 0.9)
+    sets = C.perturbed_sets(d["ab"], 8, seed=4)
+    Ob, Nb, sc = ssb.score_batch(G, g, _dev(bf), sets, _dev(band))
+    torch.cuda.synchronize()
+    Gor = O.build_G(d["frames"], bf)
+    for s, ab in enumerate(sets):
+        Oref, Nref = O.reduce(Gor, g, ab, bf, entries=band)
+        assert np.array_equal(Nb[s].cpu().numpy(), Nref)
+        assert rel(Ob[s].cpu().numpy(), Oref) < TOL
+        assert abs(sc[s].item() - O.score(Oref, Nref)) <= TOL * abs(O.score(Oref, Nref))
+
+
+def test_score_batch_B_invariance(ssb, small_G):
+    """Set s of an 8-set pass equals the single-set pass bit for bit."""
+    d, bf, G = small_G
+    g = d["geom"]
+    band = _dev(O.band_indices(g, 0.2, 0.9))
+    bfd = _dev(bf)
+    sets = C.perturbed_sets(d["ab"], 8, seed=11)
+    O8, N8, s8 = ssb.score_batch(G, g, bfd, sets, band)
+    for B in (2, 4, 5):
+        OB, NB, sB = ssb.score_batch(G, g, bfd, sets[:B], band)
+        assert torch.equal(OB, O8[:B]) and torch.equal(NB, N8[:B]) and torch.equal(sB, s8[:B])
+    for s in range(8):
+        O1, N1, s1 = ssb.score_batch(G, g, bfd, [sets[s]], band)
+        assert torch.equal(O1[0], O8[s]) and torch.equal(N1[0], N8[s]) and torch.equal(s1[0], s8[s])
+
+
+def test_score_of_matched_set_is_highest(ssb, tiny_dataset):
+    """Noiseless data: the simulated set outscores sets with defocus steps."""
+    d = tiny_dataset
+    g = d["geom"]
+    bf = O.bf_indices(g)
+    G = ssb.build_G(_frames_dev(d["frames"]), g, _dev(bf))
+    band = _dev(O.band_indices(g, 0.2, 0.9))
+    sets = [d["ab"].replace(C10=d["ab"].C10 + dz) for dz in (-40.0, -20.0, 0.0, 20.0, 40.0)]
+    _, _, sc = ssb.score_batch(G, g, _dev(bf), sets, band)
+    assert int(torch.argmax(sc)) == 2
+
+
+def test_reconstruct_is_deterministic(ssb, small_G):
+    d, bf, G = small_G
+    bfd = _dev(bf)
+    a = ssb.reconstruct(G, d["geom"], bfd, d["ab"])
+    b = ssb.reconstruct(G, d["geom"], bfd, d["ab"])
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
