@@ -39,7 +39,7 @@ def parse():
     p.add_argument("--steps", type=int, default=10)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--workload", default="full", choices=["full", "large", "small", "tiny"])
+    p.add_argument("--workload", default="full", choices=["full", "large", "mid", "small", "tiny"])
     p.add_argument("--sets", type=int, default=8)
     p.add_argument("--e2e-steps", type=int, default=3)
     p.add_argument("--no-e2e", action="store_true")
@@ -188,7 +188,7 @@ def run_reference(args, ws, rank):
     from synth import forward as F
     import torch
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    d = F.make_torch_dataset(args.workload, device=dev) if args.workload in ("full", "large") \
+    d = F.make_torch_dataset(args.workload, device=dev) if args.workload in ("full", "large", "mid") \
         else F.make_numpy_dataset(args.workload)
     g, ab = d["geom"], d["ab"]
     from oracle import ssb_oracle as O
@@ -239,7 +239,7 @@ def run_ours(args, ws, rank, local, pg):
     dev = torch.device("cuda", local)
     ssb.load()
 
-    d = F.make_torch_dataset(args.workload, device=dev) if args.workload in ("full", "large") \
+    d = F.make_torch_dataset(args.workload, device=dev) if args.workload in ("full", "large", "mid") \
         else None
     if d is None:
         dn = F.make_numpy_dataset(args.workload)

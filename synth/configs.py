@@ -16,6 +16,7 @@ Workloads (scan n x n at 0.373 A, 300 kV, 30 mrad):
 * ``batch`` B aberration sets perturbed from the ``full`` draw, scored over
   the band 0.2 <= |q| <= 0.9 1/A.
 * ``large`` as ``full`` on a 1024^2 scan.
+* ``mid``   512^2 scan with the 64^2 detector of ``small`` (profiling case).
 
 The sources for these numbers are the MoS2 / crystal scans of the quantem.gpu
 SSB reports (2026-10-24 regularized preparation, "Setup"; 2026-10-20 tilt
@@ -117,6 +118,9 @@ WORKLOADS = {
     "small": Workload("small", 1, 128, 64, 30.0 / 18.0, "u16", 5.0, "gaussians", n_atoms=120),
     "full": Workload("full", 2, 512, 192, 0.551, "u16", 3.0, "hex"),
     "large": Workload("large", 3, 1024, 192, 0.551, "u16", 3.0, "hex"),
+    # profiling case: the full scan size with the small detector (2.1 GB of
+    # frames, ~1k BF pixels) so that many-pass counter captures stay small
+    "mid": Workload("mid", 5, 512, 64, 30.0 / 18.0, "u16", 3.0, "hex"),
 }
 
 
