@@ -33,7 +33,10 @@ STATUS_NAMES = {0: "SSB_OK", 1: "SSB_INVALID_ARG", 2: "SSB_UNSUPPORTED",
                 3: "SSB_WORKSPACE_TOO_SMALL", 4: "SSB_CUDA_ERROR"}
 
 EXPORTED = ("ssb_bf_indices", "ssb_band_indices", "ssb_workspace_bytes", "ssb_build_G",
-            "ssb_reconstruct", "ssb_score_batch", "ssb_last_error", "ssb_launch_count")
+            "ssb_reconstruct", "ssb_score_batch", "ssb_last_error", "ssb_launch_count",
+            "ssb_reconstruct_noalloc")
+
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class Geometry(ctypes.Structure):
@@ -81,10 +84,11 @@ def load(path: str | None = None):
     lib.ssb_reconstruct.argtypes = [c_vp, G_p, c_vp, c_int, A_p, c_vp, c_vp, c_vp, c_vp, c_size, c_vp]
     lib.ssb_score_batch.argtypes = [c_vp, G_p, c_vp, c_int, A_p, c_int, c_vp, c_int, c_vp, c_vp, c_vp,
                                     c_vp, c_size, c_vp]
+    lib.ssb_reconstruct_noalloc.argtypes = [c_vp, G_p, c_vp, c_int, A_p, c_vp, c_vp, c_vp, c_vp]
     lib.ssb_last_error.restype = ctypes.c_char_p
     lib.ssb_launch_count.restype = ctypes.c_longlong
     for fn in ("ssb_bf_indices", "ssb_band_indices", "ssb_build_G", "ssb_reconstruct",
-               "ssb_score_batch"):
+               "ssb_score_batch", "ssb_reconstruct_noalloc"):
         getattr(lib, fn).restype = c_int
     _lib = lib
     return lib
@@ -250,3 +254,23 @@ def score_batch(G, geom, bf_idx_dev, sets, band_dev, O=None, N=None, score=None,
                                                   _ptr(band_dev), nq, _ptr(O), _ptr(N), _ptr(score),
                                                   ws.ptr(), ws.nbytes, _stream(stream)))
     return O, N, score
+
+
+def reconstruct_noalloc(G, geom, bf_idx_dev, aberr, O=None, N=None, phase=None, stream=None):
+    """ssb_reconstruct_noalloc: the reconstruction with the library's fixed
+    scratch array instead of a workspace (for callers that cannot allocate
+    device memory; the output tensors are created here only if not given)."""
+    import torch
+    lib = load()
+    g = to_geometry(geom)
+    a = to_aberr(aberr)
+    n_bf = int(bf_idx_dev.numel())
+    n, h = g.n, g.n // 2 + 1
+    dev = G.device
+    O = torch.empty((n, h), dtype=torch.complex64, device=dev) if O is None else O
+    N = torch.empty((n, h), dtype=torch.int32, device=dev) if N is None else N
+    phase = torch.empty((n, n), dtype=torch.float32, device=dev) if phase is None else phase
+    _check("ssb_reconstruct_noalloc", lib.ssb_reconstruct_noalloc(
+        _ptr(G), ctypes.byref(g), _ptr(bf_idx_dev), n_bf, ctypes.byref(a), _ptr(O), _ptr(N), _ptr(phase),
+        _stream(stream)))
+    return O, N, phase

@@ -28,6 +28,11 @@ static int cuda_fail(cudaError_t e, const char* where) {
     return fail(SSB_CUDA_ERROR, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
+int set_last_error(int code, const char* msg, cudaError_t err) {
+    if (err != cudaSuccess) return fail(code, "%s: %s (%s)", msg, cudaGetErrorName(err), cudaGetErrorString(err));
+    return fail(code, "%s", msg);
+}
+
 // IEEE double product with its own rounding, whatever the host compiler's
 // contraction settings (the BF predicate must match a plain float64 reading).
 static double mul_rn(double a, double b) {

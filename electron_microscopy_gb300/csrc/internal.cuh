@@ -221,4 +221,8 @@ cudaError_t launch_score(const float2* O, const int32_t* N, int B, int nq, doubl
 // launch bookkeeping (api.cu)
 void count_launch(int k = 1);
 
+// record `msg` (plus the CUDA error text when err != cudaSuccess) as this
+// thread's last error and return `code` (api.cu)
+int set_last_error(int code, const char* msg, cudaError_t err);
+
 }  // namespace ssb

@@ -175,6 +175,34 @@ int ssb_score_batch(const void* G_dev, const ssb_geometry* geom,
                     void* O_dev, int32_t* N_dev, double* score_dev,
                     void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * ssb_reconstruct for callers that cannot allocate device memory.
+ *
+ * No page describes this call; it has no counterpart in the method.  It exists
+ * for callers that are not allowed to call cudaMalloc or any allocating
+ * routine: plugin code running inside a host application that owns the device
+ * allocator, or acquisition loops that must not allocate once started.  It
+ * computes exactly what ssb_reconstruct computes (same kernels, same outputs,
+ * same argument meaning, layout and status codes), but its scratch memory is a
+ * fixed array of SSB_NOALLOC_SCRATCH_BYTES inside the library (held by every
+ * GPU that loads the library until the process exits) instead of a caller
+ * workspace.  It calls no allocating routine.
+ *   - Calls whose scratch need, ssb_workspace_bytes(geom, n_bf, SSB_OP_RECON,
+ *     1, 1), exceeds SSB_NOALLOC_SCRATCH_BYTES return SSB_UNSUPPORTED before
+ *     launching anything (every n <= 512 fits; n = 1024 does not).
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make that
+ *     first call before any stream capture.
+ *   - All calls share the one array, which keeps the last call's contents;
+ *     nothing in it needs to start at zero.  Calls that overlap on the GPU
+ *     (different streams or host threads) race on it: serialise them.
+ */
+#define SSB_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+int ssb_reconstruct_noalloc(const void* G_dev, const ssb_geometry* geom,
+                            const int32_t* bf_idx_dev, int n_bf, const ssb_aberr* set,
+                            void* O_dev, int32_t* N_dev, float* phase_dev, void* stream);
+
 /* Text of the last error on this host thread ("" if none). */
 const char* ssb_last_error(void);
 
