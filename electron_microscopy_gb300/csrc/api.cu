@@ -111,7 +111,7 @@ static int red_splits(int nq, int n_bf) {
 }
 
 struct WsLayout {
-    size_t tw, ktab, chik, amask, Opart, Npart, dcpart, Y, total;
+    size_t tw, xbuf, ktab, chik, amask, Opart, Npart, dcpart, Y, total;
 };
 
 static WsLayout layout(const ssb_geometry* g, int n_bf, int op, int B, int nq) {
@@ -121,6 +121,10 @@ static WsLayout layout(const ssb_geometry* g, int n_bf, int op, int B, int nq) {
     L.tw = off;
     off += align256((size_t)n * sizeof(float2));
     if (op == SSB_OP_BUILD) {
+        if (n == 512) {  // chunk buffers of the cluster build
+            L.xbuf = off;
+            off += align256(plane512_chunk_bytes());
+        }
         L.total = off;
         return L;
     }
@@ -277,9 +281,13 @@ int ssb_build_G(const void* frames, int dtype, const ssb_geometry* geom, const i
     float2* tw = at<float2>(ws, Lw.tw);
     cudaError_t e;
     if ((e = launch_twiddles(tw, geom->n, st)) != cudaSuccess) return cuda_fail(e, "twiddles");
-    if ((e = launch_build(frames, dtype, geom->n, geom->det_y * geom->det_x, bf_idx_dev, n_bf,
-                          static_cast<float2*>(G_dev), tw, st)) != cudaSuccess)
-        return cuda_fail(e, "build");
+    if (geom->n == 512 && dtype == SSB_U16 && plane512_clusters() > 0)
+        e = launch_build512(static_cast<const uint16_t*>(frames), geom->det_y * geom->det_x, bf_idx_dev, n_bf,
+                            static_cast<float2*>(G_dev), tw, at<void>(ws, Lw.xbuf), st);
+    else
+        e = launch_build(frames, dtype, geom->n, geom->det_y * geom->det_x, bf_idx_dev, n_bf,
+                         static_cast<float2*>(G_dev), tw, st);
+    if (e != cudaSuccess) return cuda_fail(e, "build");
     g_err[0] = 0;
     return SSB_OK;
 }

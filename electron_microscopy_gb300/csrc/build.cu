@@ -25,7 +25,7 @@ namespace ssb {
 // ---------------------------------------------------------------------------
 // twiddle table W[m] = exp(-2 pi i m / n), m < n, from double precision
 // ---------------------------------------------------------------------------
-__global__ void twiddle_kernel(float2* tw, int n) {
+__global__ void ssb_twiddles(float2* tw, int n) {
     int m = blockIdx.x * blockDim.x + threadIdx.x;
     if (m < n) {
         double s, c;
@@ -35,7 +35,7 @@ __global__ void twiddle_kernel(float2* tw, int n) {
 }
 
 cudaError_t launch_twiddles(float2* tw, int n, cudaStream_t st) {
-    twiddle_kernel<<<(n + 255) / 256, 256, 0, st>>>(tw, n);
+    ssb_twiddles<<<(n + 255) / 256, 256, 0, st>>>(tw, n);
     count_launch();
     return cudaGetLastError();
 }
@@ -60,7 +60,7 @@ constexpr size_t row_smem_bytes() {
 
 template <int N, typename T>
 __global__ void __launch_bounds__(kRowThreads)
-row_r2c_kernel(const T* __restrict__ frames, int det_pix, const int32_t* __restrict__ bf_idx,
+ssb_row_r2c(const T* __restrict__ frames, int det_pix, const int32_t* __restrict__ bf_idx,
                int k_begin, int k_end, float2* __restrict__ G, const float2* __restrict__ twg) {
     constexpr int L = N / 2;
     constexpr int H = N / 2 + 1;
@@ -118,7 +118,7 @@ constexpr size_t col_smem_bytes() {
 
 template <int N>
 __global__ void __launch_bounds__(kColThreads)
-col_c2c_kernel(float2* __restrict__ G, int k_begin, const float2* __restrict__ twg) {
+ssb_col_c2c(float2* __restrict__ G, int k_begin, const float2* __restrict__ twg) {
     constexpr int H = N / 2 + 1;
     constexpr int CW = col_width<N>();
     constexpr int NG = (N / 2) / CW;
@@ -157,10 +157,10 @@ static cudaError_t build_n(const T* frames, int det_pix, const int32_t* bf_idx, 
                            float2* G, const float2* tw, cudaStream_t st) {
     const size_t rs = row_smem_bytes<N>(), cs = col_smem_bytes<N>();
     cudaError_t e;
-    if ((e = cudaFuncSetAttribute(row_r2c_kernel<N, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((e = cudaFuncSetAttribute(ssb_row_r2c<N, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)rs)) != cudaSuccess)
         return e;
-    if ((e = cudaFuncSetAttribute(col_c2c_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((e = cudaFuncSetAttribute(ssb_col_c2c<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)cs)) != cudaSuccess)
         return e;
     // chunk of BF pixels whose intermediate rows (chunk * n * (n/2+1) * 8 B)
@@ -174,18 +174,18 @@ static cudaError_t build_n(const T* frames, int det_pix, const int32_t* bf_idx, 
         if (kb < n_bf) {
             const int ke = kb + chunk < n_bf ? kb + chunk : n_bf;
             dim3 grid(N, (ke - kb + kRowPix - 1) / kRowPix);
-            row_r2c_kernel<N, T><<<grid, kRowThreads, rs, st>>>(frames, det_pix, bf_idx, kb, ke, G, tw);
+            ssb_row_r2c<N, T><<<grid, kRowThreads, rs, st>>>(frames, det_pix, bf_idx, kb, ke, G, tw);
             count_launch();
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
             if (prev_b >= 0) {
-                col_c2c_kernel<N><<<dim3(NG, prev_e - prev_b), kColThreads, cs, st>>>(G, prev_b, tw);
+                ssb_col_c2c<N><<<dim3(NG, prev_e - prev_b), kColThreads, cs, st>>>(G, prev_b, tw);
                 count_launch();
                 if ((e = cudaGetLastError()) != cudaSuccess) return e;
             }
             prev_b = kb;
             prev_e = ke;
         } else {
-            col_c2c_kernel<N><<<dim3(NG, prev_e - prev_b), kColThreads, cs, st>>>(G, prev_b, tw);
+            ssb_col_c2c<N><<<dim3(NG, prev_e - prev_b), kColThreads, cs, st>>>(G, prev_b, tw);
             count_launch();
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
             prev_b = -1;

@@ -79,6 +79,60 @@ template <> struct Dft<8> {
     }
 };
 
+// multiply by W16^M = exp(-2 pi i M / 16), trivial factors written out
+template <int M>
+__device__ __forceinline__ float2 w16(float2 a) {
+    constexpr float c1 = 0.92387953251128676f;  // cos(pi/8)
+    constexpr float s1 = 0.38268343236508977f;  // sin(pi/8)
+    constexpr float h = 0.70710678118654752f;
+    if constexpr (M == 0) {
+        return a;
+    } else if constexpr (M == 1) {  // (c1, -s1)
+        return make_float2(c1 * a.x + s1 * a.y, c1 * a.y - s1 * a.x);
+    } else if constexpr (M == 2) {  // (h, -h)
+        return make_float2(h * (a.x + a.y), h * (a.y - a.x));
+    } else if constexpr (M == 3) {  // (s1, -c1)
+        return make_float2(s1 * a.x + c1 * a.y, s1 * a.y - c1 * a.x);
+    } else if constexpr (M == 4) {  // -i
+        return cmul_mi(a);
+    } else if constexpr (M == 6) {  // (-h, -h)
+        return make_float2(h * (a.y - a.x), -h * (a.x + a.y));
+    } else {                        // M == 9: (-c1, s1)
+        static_assert(M == 9, "only the factors of a 4x4 split are needed");
+        return make_float2(-c1 * a.x - s1 * a.y, s1 * a.x - c1 * a.y);
+    }
+}
+
+template <> struct Dft<16> {
+    // 16 = 4 x 4: radix-4 over n2 for each n1 (input index n1 + 4 n2), twiddle
+    // W16^(n1 k2), radix-4 over n1; output index k2 + 4 k1.
+    static __device__ __forceinline__ void run(float2* v) {
+        float2 a0[4] = {v[0], v[4], v[8], v[12]};
+        float2 a1[4] = {v[1], v[5], v[9], v[13]};
+        float2 a2[4] = {v[2], v[6], v[10], v[14]};
+        float2 a3[4] = {v[3], v[7], v[11], v[15]};
+        Dft<4>::run(a0);
+        Dft<4>::run(a1);
+        Dft<4>::run(a2);
+        Dft<4>::run(a3);
+        float2 b0[4] = {a0[0], a1[0], a2[0], a3[0]};
+        float2 b1[4] = {a0[1], w16<1>(a1[1]), w16<2>(a2[1]), w16<3>(a3[1])};
+        float2 b2[4] = {a0[2], w16<2>(a1[2]), w16<4>(a2[2]), w16<6>(a3[2])};
+        float2 b3[4] = {a0[3], w16<3>(a1[3]), w16<6>(a2[3]), w16<9>(a3[3])};
+        Dft<4>::run(b0);
+        Dft<4>::run(b1);
+        Dft<4>::run(b2);
+        Dft<4>::run(b3);
+#pragma unroll
+        for (int k1 = 0; k1 < 4; ++k1) {
+            v[0 + 4 * k1] = b0[k1];
+            v[1 + 4 * k1] = b1[k1];
+            v[2 + 4 * k1] = b2[k1];
+            v[3 + 4 * k1] = b3[k1];
+        }
+    }
+};
+
 // ---------------------------------------------------------------------------
 // warp-level in-place Stockham pass over a row of L points in shared memory.
 // NS: span of the sub-transforms already done; TWS: stride into the
@@ -191,6 +245,13 @@ cudaError_t launch_twiddles(float2* tw, int n, cudaStream_t st);
 cudaError_t launch_build(const void* frames, int dtype, int n, int det_pix,
                          const int32_t* bf_idx, int n_bf, float2* G, const float2* tw,
                          cudaStream_t st);
+// n = 512, uint16 frames: gather + cluster FFT (plane.cu); xbuf holds
+// plane512_chunk_bytes(); plane512_clusters() is 0 when the cluster kernel
+// cannot be scheduled on the current device
+size_t plane512_chunk_bytes();
+int plane512_clusters();
+cudaError_t launch_build512(const uint16_t* frames, int det_pix, const int32_t* bf_idx, int n_bf,
+                            float2* G, const float2* tw, void* xbuf, cudaStream_t st);
 
 struct RedLaunch {
     const float2* G;

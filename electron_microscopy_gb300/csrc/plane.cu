@@ -1,0 +1,466 @@
+// plane.cu -- G(q,k) build for the n = 512 scan: gather + one-pass 2D R2C on a
+// thread-block cluster.
+//
+// What is computed is the same as build.cu (G(q,k) = sum_r x_k(r)
+// exp(-2 pi i (f_y r_y + f_x r_x)/n), half plane [k][q_y][q_x]; quantem.gpu
+// "Historical WebGPU G(q,k) memory experiment", sections "Why herm is exactly
+// lossless" and "Implementation"); how differs:
+//
+//  1. ssb_gather: for a chunk of up to 64 bright-field pixels, reads the frames
+//     once (each warp load takes 32 neighbouring detector pixels of one frame,
+//     16-32 loads in flight per thread, streaming cache hint) and writes the
+//     transposed traces X[pixel][r] (uint16, or float for float frames) into a
+//     chunk buffer that stays in L2 for the next kernel.
+//  2. ssb_plane512: one cluster of 8 CTAs per bright-field pixel (persistent:
+//     as many clusters as fit, each looping over planes).  CTA j owns scan
+//     rows r_y = j + 8 m (m < 64):
+//       a. real-to-complex FFT of each of its 64 rows along r_x: a 256-point
+//          complex FFT of the packed even/odd samples (16 threads per row,
+//          two radix-16 passes, one shared-memory transpose) and the split
+//          step, into a 64 x 257 slab in shared memory;
+//       b. for each of the 257 columns, the 64-point DFT over its own rows,
+//          times exp(-2 pi i j k_lo / 512) (8 threads per column, radix 8 x 8);
+//       c. the 64 x 257 results go to an L2-resident exchange slot of the
+//          cluster; cluster barrier; then the last radix-8 stage across the 8
+//          CTAs: CTA j reads the 8 CTAs' entries (k_lo, q_x) for k_lo in
+//          [8j, 8j+8) from L2 and writes G[k][k_lo + 64 k_hi][q_x] straight
+//          to HBM, once.  (Reading the slabs through distributed shared
+//          memory instead measured ~34 GB/s per SM, 3x slower than L2.)
+//     The chunk buffer lines it consumed are dropped from L2 without being
+//     written back (discard.global.L2): they are dead.
+// The HBM traffic of a build is therefore the frames read once plus G
+// written once; the n x (n/2+1) intermediate stays on chip (shared memory
+// and L2).
+#include <mutex>
+
+#include "internal.cuh"
+
+namespace ssb {
+
+constexpr int kGatherThreads = 256;
+constexpr int kGatherFrames = 128;  // scan positions per gather CTA
+
+template <typename T>
+__host__ __device__ constexpr int gather_pixels() { return sizeof(T) == 2 ? 64 : 32; }
+
+// ---------------------------------------------------------------------------
+// gather: frames (npos, det_pix) -> X[p][r] for p < kc, r in this CTA's block
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(kGatherThreads)
+ssb_gather(const T* __restrict__ frames, int det_pix, const int32_t* __restrict__ bf_idx, int k0, int kc,
+           int npos, T* __restrict__ X) {
+    constexpr int KC = gather_pixels<T>();
+    constexpr int FS = kGatherThreads / KC;          // frame slots per pass
+    constexpr int NL = kGatherFrames / FS;           // loads per thread
+    constexpr int PAD = sizeof(T) == 2 ? 2 : 1;      // odd word stride between rows
+    constexpr int RS = kGatherFrames + PAD;
+    __shared__ __align__(16) T s[KC * RS];
+    const int tid = threadIdx.x;
+    const int p = tid % KC, fs = tid / KC;
+    const int f0 = blockIdx.x * kGatherFrames;
+    if (p < kc) {
+        const T* src = frames + (size_t)(f0 + fs) * det_pix + bf_idx[k0 + p];
+        T v[NL];
+#pragma unroll
+        for (int i = 0; i < NL; ++i) v[i] = __ldcs(src + (size_t)(FS * i) * det_pix);
+#pragma unroll
+        for (int i = 0; i < NL; ++i) s[p * RS + fs + FS * i] = v[i];
+    }
+    __syncthreads();
+    // write rows of kGatherFrames elements as 16-byte vectors
+    constexpr int VE = 16 / (int)sizeof(T);
+    constexpr int VPR = kGatherFrames / VE;
+    for (int idx = tid; idx < kc * VPR; idx += kGatherThreads) {
+        const int row = idx / VPR, col = idx - row * VPR;
+        const T* r = s + row * RS + col * VE;
+        uint4 pk;
+        if constexpr (sizeof(T) == 2) {
+            const uint32_t* w = reinterpret_cast<const uint32_t*>(r);  // 4-byte aligned: RS even
+            pk = make_uint4(w[0], w[1], w[2], w[3]);
+        } else {
+            pk = make_uint4(__float_as_uint(r[0]), __float_as_uint(r[1]), __float_as_uint(r[2]),
+                            __float_as_uint(r[3]));
+        }
+        *reinterpret_cast<uint4*>(X + (size_t)row * npos + f0 + col * VE) = pk;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// cluster helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// cluster barrier without release semantics: for the end of a phase whose
+// only cross-CTA accesses were reads that have already completed
+__device__ __forceinline__ void cluster_sync_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+__device__ __forceinline__ void discard_l2_line(const void* p) {
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
+// packed even/odd samples z = (x[2w], x[2w+1]) / 2 from one 32-bit word of
+// two uint16 counts: 2^23 + u is exact in float, (2^23 + u)/2 - 2^22 = u/2
+__device__ __forceinline__ float2 half_pair(uint32_t u) {
+    const float lo = __fmaf_rn(__uint_as_float(0x4B000000u | (u & 0xFFFFu)), 0.5f, -4194304.0f);
+    const float hi = __fmaf_rn(__uint_as_float(0x4B000000u | (u >> 16)), 0.5f, -4194304.0f);
+    return make_float2(lo, hi);
+}
+
+// ---------------------------------------------------------------------------
+// one bright-field pixel's 512 x 512 real-to-complex FFT on an 8-CTA cluster;
+// persistent: cluster c handles chunk planes c, c + nclusters, ...
+// ---------------------------------------------------------------------------
+constexpr int kPlaneN = 512;
+constexpr int kPlaneC = 8;                 // CTAs per cluster
+constexpr int kPlaneM = kPlaneN / kPlaneC; // scan rows per CTA
+constexpr int kPlaneH = kPlaneN / 2 + 1;
+constexpr int kPlanePS = 258;              // slab row stride (float2); 258 = 2 mod 16: conflict-free columns
+constexpr int kPlaneThreads = 512;
+// shared memory: split-step twiddles W512^k (k <= 256), row twiddles
+// W256^(t k2) laid out [k2][t], column twiddles W64^(t k2) laid out [k2][t],
+// cross twiddles W512^(j k_lo), then the 64 x PS slab
+constexpr int kTwSplit = 0, kTwRow = 260, kTwCol = kTwRow + 256, kTwCross = kTwCol + 64, kTwTotal = kTwCross + 64;
+// staged uint16 rows of the next plane: row stride 544 (16 words mod 32, so the
+// two half-warps reading adjacent rows hit disjoint banks; 16-byte aligned)
+constexpr int kStageRS = 544;
+// cross-CTA exchange through L2: per cluster slot, [rank][k_lo][kXchRS] float2
+constexpr int kXchRS = 264;  // 32-byte aligned rows
+constexpr size_t kXchSlot = (size_t)kPlaneC * kPlaneM * kXchRS * sizeof(float2);
+constexpr int kMaxClusters = 24;
+constexpr size_t kSlabBytes = (size_t)kPlaneM * kPlanePS * sizeof(float2);
+constexpr size_t kPlaneSmem = (size_t)kTwTotal * sizeof(float2) + kSlabBytes + (size_t)kPlaneM * kStageRS * 2;
+
+// stage the 64 rows r_y = j + 8 m of plane Xk: thread i copies 128-byte line
+// i % 8 of row i / 8 (eight 16-byte cp.async)
+__device__ __forceinline__ void stage_rows(const uint16_t* Xk, uint32_t stage, uint32_t j, int tid) {
+    const int m = tid >> 3, l = tid & 7;
+    const char* src = reinterpret_cast<const char*>(Xk + (size_t)(j + kPlaneC * m) * kPlaneN) + 128 * l;
+    const uint32_t dst = stage + (uint32_t)(m * kStageRS * 2 + 128 * l);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) cp_async16(dst + 16 * c, src + 16 * c);
+    cp_async_commit();
+}
+
+__global__ void __launch_bounds__(kPlaneThreads, 1)
+ssb_plane512(const uint16_t* __restrict__ X, int k0, int kc, float2* __restrict__ G, const float2* __restrict__ twg,
+             float2* __restrict__ xch) {
+    constexpr int N = kPlaneN, H = kPlaneH, PS = kPlanePS;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    float2* tws = reinterpret_cast<float2*>(smem_raw);
+    float2* slab = tws + kTwTotal;  // [64][PS]
+    const uint32_t* stg = reinterpret_cast<const uint32_t*>(smem_raw + kTwTotal * sizeof(float2) + kSlabBytes);
+    const uint32_t stage = smem_addr(stg);
+    const int tid = threadIdx.x;
+    const uint32_t j = cluster_rank();
+    const int ncl = gridDim.x / kPlaneC;
+    int kk = blockIdx.x / kPlaneC;
+    if (kk < kc) stage_rows(X + (size_t)kk * N * N, stage, j, tid);
+
+    for (int i = tid; i < kTwTotal; i += kPlaneThreads) {
+        float2 w = make_float2(1.f, 0.f);
+        if (i < kTwRow) {
+            if (i <= N / 2) w = twg[i];
+        } else if (i < kTwCol) {
+            const int k2 = (i - kTwRow) >> 4, t = (i - kTwRow) & 15;
+            w = twg[2 * t * k2];
+        } else if (i < kTwCross) {
+            const int k2 = (i - kTwCol) >> 3, t = (i - kTwCol) & 7;
+            w = twg[8 * t * k2];
+        } else {
+            w = twg[j * (i - kTwCross)];
+        }
+        tws[i] = w;
+    }
+
+#pragma unroll 1
+    for (; kk < kc; kk += ncl) {
+        // this thread's staged line has landed; its global copy is dead: drop it
+        // from L2 without write-back
+        cp_async_wait_all();
+        discard_l2_line(reinterpret_cast<const char*>(X + (size_t)kk * N * N + (size_t)(j + kPlaneC * (tid >> 3)) * N) +
+                        128 * (tid & 7));
+        __syncthreads();
+        // ---- a. row R2C: 16 threads per row, 32 rows at a time ----
+        {
+            const int t = tid & 15, hw = tid >> 4;
+            const int lane = tid & 31;
+            const int src_lane = (lane & 16) | ((16 - t) & 15);
+#pragma unroll 1
+            for (int it = 0; it < kPlaneM / 32; ++it) {
+                const int m = it * 32 + hw;
+                const uint32_t* row = stg + m * (kStageRS / 2);
+                float2 v[16];
+#pragma unroll
+                for (int n2 = 0; n2 < 16; ++n2) v[n2] = half_pair(row[t + 16 * n2]);
+                Dft<16>::run(v);
+#pragma unroll
+                for (int k2 = 1; k2 < 16; ++k2) v[k2] = cmul(v[k2], tws[kTwRow + 16 * k2 + t]);  // W256^(t k2)
+                float2* s = slab + m * PS;
+#pragma unroll
+                for (int k2 = 0; k2 < 16; ++k2) s[k2 * 16 + (t ^ k2)] = v[k2];
+                __syncwarp();
+#pragma unroll
+                for (int n1 = 0; n1 < 16; ++n1) v[n1] = s[t * 16 + (n1 ^ t)];
+                __syncwarp();
+                Dft<16>::run(v);  // v[k1] = Z[t + 16 k1] (Z of the halved samples)
+                // split step: X[k] = a - i W^k b, a = Z[k] + conj Z[L-k], b = Z[k] - conj Z[L-k]
+#pragma unroll
+                for (int k1 = 0; k1 < 16; ++k1) {
+                    float2 pr;
+                    pr.x = __shfl_sync(0xffffffffu, v[15 - k1].x, src_lane);
+                    pr.y = __shfl_sync(0xffffffffu, v[15 - k1].y, src_lane);
+                    if (t == 0) pr = v[(16 - k1) & 15];
+                    const float2 z = v[k1];
+                    const float ax = z.x + pr.x, ay = z.y - pr.y;
+                    const float bx = z.x - pr.x, by = z.y + pr.y;
+                    const float2 w = tws[kTwSplit + t + 16 * k1];
+                    s[t + 16 * k1] = make_float2(ax + w.x * by + w.y * bx, ay - w.x * bx + w.y * by);
+                }
+                if (t == 0) s[N / 2] = make_float2(2.0f * (v[0].x - v[0].y), 0.0f);
+            }
+        }
+        __syncthreads();
+        // the staging buffer is free: fetch the next plane while this one finishes
+        if (kk + ncl < kc) stage_rows(X + (size_t)(kk + ncl) * N * N, stage, j, tid);
+        // ---- b. local 64-point column DFTs, times W512^(j k_lo), to the L2 exchange ----
+        // Thread (t, c): lanes span 32 consecutive columns, t = warp / 2 picks
+        // the 8-point sub-sequence; the 8 x 8 transposition goes through the
+        // column's own slab rows between block barriers.
+        float2* xmine = xch + (size_t)(blockIdx.x / kPlaneC) * (kXchSlot / sizeof(float2));
+        {
+            float2* xout = xmine + (size_t)j * kPlaneM * kXchRS;
+            const int t = tid >> 6, cl = tid & 63;
+            float2 wc[8], wx[8];
+#pragma unroll
+            for (int k2 = 0; k2 < 8; ++k2) {
+                wc[k2] = tws[kTwCol + 8 * k2 + t];    // W64^(t k2)
+                wx[k2] = tws[kTwCross + t + 8 * k2];  // W512^(j (t + 8 k2))
+            }
+            auto col_in = [&](int c, float2* v) {
+#pragma unroll
+                for (int n2 = 0; n2 < 8; ++n2) v[n2] = slab[(t + 8 * n2) * PS + c];
+                Dft<8>::run(v);
+#pragma unroll
+                for (int k2 = 1; k2 < 8; ++k2) v[k2] = cmul(v[k2], wc[k2]);
+            };
+            auto col_out = [&](int c, float2* v) {
+#pragma unroll
+                for (int n1 = 0; n1 < 8; ++n1) v[n1] = slab[(t * 8 + (n1 ^ t)) * PS + c];
+                Dft<8>::run(v);  // v[k1] = Y[t + 8 k1]
+#pragma unroll
+                for (int k1 = 0; k1 < 8; ++k1) xout[(t + 8 * k1) * kXchRS + c] = cmul(v[k1], wx[k1]);
+            };
+#pragma unroll 1
+            for (int c = cl; c < N / 2; c += 64) {
+                float2 v[8];
+                col_in(c, v);
+                __syncthreads();
+#pragma unroll
+                for (int k2 = 0; k2 < 8; ++k2) slab[(k2 * 8 + (t ^ k2)) * PS + c] = v[k2];
+                __syncthreads();
+                col_out(c, v);
+            }
+            // column q_x = n/2: lanes 0..7 of warp 0, t = lane
+            if (tid < 8) {
+                const int tt = tid;
+                float2 v[8];
+#pragma unroll
+                for (int n2 = 0; n2 < 8; ++n2) v[n2] = slab[(tt + 8 * n2) * PS + N / 2];
+                Dft<8>::run(v);
+#pragma unroll
+                for (int k2 = 1; k2 < 8; ++k2) v[k2] = cmul(v[k2], tws[kTwCol + 8 * k2 + tt]);
+#pragma unroll
+                for (int k2 = 0; k2 < 8; ++k2) slab[(k2 * 8 + (tt ^ k2)) * PS + N / 2] = v[k2];
+                __syncwarp(0xFFu);
+#pragma unroll
+                for (int n1 = 0; n1 < 8; ++n1) v[n1] = slab[(tt * 8 + (n1 ^ tt)) * PS + N / 2];
+                Dft<8>::run(v);
+#pragma unroll
+                for (int k1 = 0; k1 < 8; ++k1)
+                    xout[(tt + 8 * k1) * kXchRS + N / 2] = cmul(v[k1], tws[kTwCross + tt + 8 * k1]);
+            }
+        }
+        __syncthreads();
+        cluster_sync();  // exchange rows written and visible to the cluster
+        // ---- c. radix-8 across the cluster, straight to G ----
+        {
+            float2* Gk = G + (size_t)(k0 + kk) * N * H;
+            auto pair = [&](int p) {
+                const int kl = 8 * (int)j + p / H, c = p % H;
+                const float2* src = xmine + (size_t)kl * kXchRS + c;
+                float2 v[8];
+#pragma unroll
+                for (int r = 0; r < kPlaneC; ++r) v[r] = __ldcg(src + (size_t)r * kPlaneM * kXchRS);
+                Dft<8>::run(v);
+#pragma unroll
+                for (int kh = 0; kh < 8; ++kh) __stcs(Gk + (size_t)(kl + 64 * kh) * H + c, v[kh]);
+            };
+            constexpr int P = 8 * H;                               // 2056 (k_lo, q_x) pairs
+            constexpr int PFULL = (P / (2 * kPlaneThreads)) * 2 * kPlaneThreads;  // 2048
+#pragma unroll 1
+            for (int p = tid; p < PFULL; p += 2 * kPlaneThreads) {
+                pair(p);
+                pair(p + kPlaneThreads);
+            }
+            if (PFULL + tid < P) pair(PFULL + tid);
+        }
+        cluster_sync_relaxed();  // every read of this cluster's exchange rows has completed
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+// co-resident 8-CTA clusters of ssb_plane512 on this device (cached per device)
+static int plane_clusters() {
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cached[dev] > 0) return cached[dev];
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kPlaneC;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(kPlaneC, 1, 1);
+    cfg.blockDim = dim3(kPlaneThreads, 1, 1);
+    cfg.dynamicSmemBytes = kPlaneSmem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int ncl = 0;
+    if (cudaOccupancyMaxActiveClusters(&ncl, ssb_plane512, &cfg) != cudaSuccess) ncl = 0;
+    cached[dev] = ncl;
+    return ncl;
+}
+
+int plane512_clusters() {
+    if (cudaFuncSetAttribute(ssb_plane512, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPlaneSmem) !=
+        cudaSuccess)
+        return 0;
+    return plane_clusters();
+}
+
+// two gather buffers of 64 planes, then the exchange slots
+size_t plane512_chunk_bytes() {
+    return (size_t)2 * 64 * kPlaneN * kPlaneN * sizeof(uint16_t) + (size_t)kMaxClusters * kXchSlot;
+}
+
+// Two internal streams per device (gather, plane) and the events that order
+// them, created on first use; the launch sequence of one build holds the
+// device's mutex so that concurrent builds cannot interleave their events.
+struct BuildStreams {
+    cudaStream_t sg = nullptr, sp = nullptr;
+    cudaEvent_t fork = nullptr, g_done[2] = {}, p_done[2] = {};
+    std::mutex mu;
+    bool ready = false;
+};
+
+static cudaError_t get_streams(BuildStreams** out) {
+    static BuildStreams per_dev[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    BuildStreams& b = per_dev[dev];
+    {
+        std::lock_guard<std::mutex> lock(b.mu);
+        if (!b.ready) {
+            int lo = 0, hi = 0;
+            if ((e = cudaDeviceGetStreamPriorityRange(&lo, &hi)) != cudaSuccess) return e;
+            if ((e = cudaStreamCreateWithPriority(&b.sg, cudaStreamNonBlocking, lo)) != cudaSuccess) return e;
+            if ((e = cudaStreamCreateWithPriority(&b.sp, cudaStreamNonBlocking, hi)) != cudaSuccess) return e;
+            if ((e = cudaEventCreateWithFlags(&b.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+            for (int i = 0; i < 2; ++i) {
+                if ((e = cudaEventCreateWithFlags(&b.g_done[i], cudaEventDisableTiming)) != cudaSuccess) return e;
+                if ((e = cudaEventCreateWithFlags(&b.p_done[i], cudaEventDisableTiming)) != cudaSuccess) return e;
+            }
+            b.ready = true;
+        }
+    }
+    *out = &b;
+    return cudaSuccess;
+}
+
+cudaError_t launch_build512(const uint16_t* frames, int det_pix, const int32_t* bf_idx, int n_bf, float2* G,
+                            const float2* tw, void* xbuf, cudaStream_t st) {
+    constexpr int KCMAX = gather_pixels<uint16_t>();
+    const int npos = kPlaneN * kPlaneN;
+    cudaError_t e;
+    if ((e = cudaFuncSetAttribute(ssb_plane512, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)kPlaneSmem)) != cudaSuccess)
+        return e;
+    int ncl = plane_clusters();
+    if (ncl < 1) return cudaErrorLaunchOutOfResources;
+    if (ncl > kMaxClusters) ncl = kMaxClusters;
+    BuildStreams* bs = nullptr;
+    if ((e = get_streams(&bs)) != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(bs->mu);
+    // planes per chunk: a multiple of the co-resident clusters, at most KCMAX
+    const int KC = ncl >= KCMAX ? KCMAX : ncl * (KCMAX / ncl);
+    uint16_t* xb[2] = {static_cast<uint16_t*>(xbuf), static_cast<uint16_t*>(xbuf) + (size_t)KCMAX * npos};
+    float2* xch = reinterpret_cast<float2*>(static_cast<uint16_t*>(xbuf) + (size_t)2 * KCMAX * npos);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kPlaneC;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    // fork from the caller's stream
+    if ((e = cudaEventRecord(bs->fork, st)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(bs->sg, bs->fork, 0)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(bs->sp, bs->fork, 0)) != cudaSuccess) return e;
+    int c = 0;
+    for (int k0 = 0; k0 < n_bf; ++c, k0 += KC) {
+        const int kc = n_bf - k0 < KC ? n_bf - k0 : KC;
+        const int b = c & 1;
+        uint16_t* Xc = xb[b];
+        // gather(c) may overwrite buffer b once plane(c - 2) has read it
+        if (c >= 2 && (e = cudaStreamWaitEvent(bs->sg, bs->p_done[b], 0)) != cudaSuccess) return e;
+        ssb_gather<uint16_t><<<npos / kGatherFrames, kGatherThreads, 0, bs->sg>>>(frames, det_pix, bf_idx, k0, kc,
+                                                                                 npos, Xc);
+        count_launch();
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = cudaEventRecord(bs->g_done[b], bs->sg)) != cudaSuccess) return e;
+        if ((e = cudaStreamWaitEvent(bs->sp, bs->g_done[b], 0)) != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg = {};
+        const int grid_cl = kc < ncl ? kc : ncl;
+        cfg.gridDim = dim3(grid_cl * kPlaneC, 1, 1);
+        cfg.blockDim = dim3(kPlaneThreads, 1, 1);
+        cfg.dynamicSmemBytes = kPlaneSmem;
+        cfg.stream = bs->sp;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if ((e = cudaLaunchKernelEx(&cfg, ssb_plane512, (const uint16_t*)Xc, k0, kc, G, tw, xch)) != cudaSuccess)
+            return e;
+        count_launch();
+        if ((e = cudaEventRecord(bs->p_done[b], bs->sp)) != cudaSuccess) return e;
+    }
+    // join: the caller's stream waits for the last plane (which follows every
+    // gather through the event chain)
+    if ((e = cudaStreamWaitEvent(st, bs->p_done[(c - 1) & 1], 0)) != cudaSuccess) return e;
+    return cudaSuccess;
+}
+
+}  // namespace ssb

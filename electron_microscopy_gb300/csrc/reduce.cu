@@ -21,7 +21,7 @@ namespace ssb {
 // ---------------------------------------------------------------------------
 // k-only tables: float32 k, aperture bit per set, chi_s(k) in turns
 // ---------------------------------------------------------------------------
-__global__ void prep_kernel(const int32_t* __restrict__ bf_idx, int n_bf, int det_x, double cy,
+__global__ void ssb_prep(const int32_t* __restrict__ bf_idx, int n_bf, int det_x, double cy,
                             double cx, double dk, SetBatch sb, float4* __restrict__ ktab,
                             float* __restrict__ chik, uint32_t* __restrict__ amask) {
     const int k = blockIdx.x * blockDim.x + threadIdx.x;
@@ -44,7 +44,7 @@ __global__ void prep_kernel(const int32_t* __restrict__ bf_idx, int n_bf, int de
 cudaError_t launch_prep(const int32_t* bf_idx, int n_bf, int det_x, double cy, double cx, double dk,
                         const SetBatch& sb, float4* ktab, float* chik, uint32_t* amask,
                         cudaStream_t st) {
-    prep_kernel<<<(n_bf + 255) / 256, 256, 0, st>>>(bf_idx, n_bf, det_x, cy, cx, dk, sb, ktab, chik,
+    ssb_prep<<<(n_bf + 255) / 256, 256, 0, st>>>(bf_idx, n_bf, det_x, cy, cx, dk, sb, ktab, chik,
                                                     amask);
     count_launch();
     return cudaGetLastError();
@@ -57,7 +57,7 @@ constexpr int kRedThreads = 256;
 
 template <int MAXB>
 __global__ void __launch_bounds__(kRedThreads)
-reduce_kernel(RedLaunch P, SetBatch sb) {
+ssb_reduce(RedLaunch P, SetBatch sb) {
     const int qi = blockIdx.x * kRedThreads + threadIdx.x;
     const int split = blockIdx.y;
     const int kb = split * P.kps;
@@ -129,13 +129,13 @@ reduce_kernel(RedLaunch P, SetBatch sb) {
 cudaError_t launch_reduce(const RedLaunch& P, const SetBatch& sb, cudaStream_t st) {
     dim3 grid((P.nq + kRedThreads - 1) / kRedThreads, P.nsplit);
     if (sb.B == 1)
-        reduce_kernel<1><<<grid, kRedThreads, 0, st>>>(P, sb);
+        ssb_reduce<1><<<grid, kRedThreads, 0, st>>>(P, sb);
     else if (sb.B == 2)
-        reduce_kernel<2><<<grid, kRedThreads, 0, st>>>(P, sb);
+        ssb_reduce<2><<<grid, kRedThreads, 0, st>>>(P, sb);
     else if (sb.B <= 4)
-        reduce_kernel<4><<<grid, kRedThreads, 0, st>>>(P, sb);
+        ssb_reduce<4><<<grid, kRedThreads, 0, st>>>(P, sb);
     else
-        reduce_kernel<8><<<grid, kRedThreads, 0, st>>>(P, sb);
+        ssb_reduce<8><<<grid, kRedThreads, 0, st>>>(P, sb);
     count_launch();
     return cudaGetLastError();
 }
@@ -143,7 +143,7 @@ cudaError_t launch_reduce(const RedLaunch& P, const SetBatch& sb, cudaStream_t s
 // ---------------------------------------------------------------------------
 // partial sums -> O, N (fixed order over splits)
 // ---------------------------------------------------------------------------
-__global__ void finalize_kernel(const float2* __restrict__ Opart, const int* __restrict__ Npart,
+__global__ void ssb_finalize(const float2* __restrict__ Opart, const int* __restrict__ Npart,
                                 int nsplit, int B, int nq, float2* __restrict__ O,
                                 int32_t* __restrict__ N) {
     const size_t t = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -164,7 +164,7 @@ __global__ void finalize_kernel(const float2* __restrict__ Opart, const int* __r
 cudaError_t launch_finalize(const float2* Opart, const int* Npart, int nsplit, int B, int nq,
                             float2* O, int32_t* N, cudaStream_t st) {
     const size_t total = (size_t)B * nq;
-    finalize_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(Opart, Npart, nsplit, B, nq, O, N);
+    ssb_finalize<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(Opart, Npart, nsplit, B, nq, O, N);
     count_launch();
     return cudaGetLastError();
 }
@@ -178,7 +178,7 @@ constexpr int kPhaseThreads = 256;
 
 template <int N>
 __global__ void __launch_bounds__(kPhaseThreads)
-c2r_cols_kernel(const float2* __restrict__ O, const int32_t* __restrict__ Nn, float2* __restrict__ Y,
+ssb_c2r_cols(const float2* __restrict__ O, const int32_t* __restrict__ Nn, float2* __restrict__ Y,
                 const float2* __restrict__ twg) {
     constexpr int H = N / 2 + 1;
     constexpr int CW = (N / 2 >= 16) ? 16 : N / 2;
@@ -217,7 +217,7 @@ c2r_cols_kernel(const float2* __restrict__ O, const int32_t* __restrict__ Nn, fl
 
 template <int N>
 __global__ void __launch_bounds__(kPhaseThreads)
-c2r_rows_kernel(const float2* __restrict__ Y, const double* __restrict__ dcpart, int nsplit, int n_bf,
+ssb_c2r_rows(const float2* __restrict__ Y, const double* __restrict__ dcpart, int nsplit, int n_bf,
                 const float2* __restrict__ twg, float* __restrict__ phase) {
     constexpr int L = N / 2;
     constexpr int H = N / 2 + 1;
@@ -269,14 +269,14 @@ static cudaError_t phase_n(const float2* O, const int32_t* Nn, const double* dcp
     const size_t cs = (size_t)N * sizeof(float2) + (size_t)(CW + 1) * (N + 1) * sizeof(float2);
     const size_t rs = (size_t)N * sizeof(float2) + (size_t)(kPhaseThreads / 32) * (N / 2) * sizeof(float2);
     cudaError_t e;
-    if ((e = cudaFuncSetAttribute(c2r_cols_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((e = cudaFuncSetAttribute(ssb_c2r_cols<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)cs)) != cudaSuccess)
         return e;
-    c2r_cols_kernel<N><<<NG, kPhaseThreads, cs, st>>>(O, Nn, Y, tw);
+    ssb_c2r_cols<N><<<NG, kPhaseThreads, cs, st>>>(O, Nn, Y, tw);
     count_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     constexpr int RPB = kPhaseThreads / 32;
-    c2r_rows_kernel<N><<<(N + RPB - 1) / RPB, kPhaseThreads, rs, st>>>(Y, dcpart, nsplit, n_bf, tw, phase);
+    ssb_c2r_rows<N><<<(N + RPB - 1) / RPB, kPhaseThreads, rs, st>>>(Y, dcpart, nsplit, n_bf, tw, phase);
     count_launch();
     return cudaGetLastError();
 }
@@ -299,7 +299,7 @@ cudaError_t launch_phase(const float2* O, const int32_t* Nn, const double* dcpar
 // ---------------------------------------------------------------------------
 // score_s = sum_q |O_s(q)|^2 / sum_q N_s(q), one block per set, float64 sums
 // ---------------------------------------------------------------------------
-__global__ void score_kernel(const float2* __restrict__ O, const int32_t* __restrict__ Nn, int nq,
+__global__ void ssb_score(const float2* __restrict__ O, const int32_t* __restrict__ Nn, int nq,
                              double* __restrict__ score) {
     __shared__ double s_num[256];
     __shared__ long long s_den[256];
@@ -326,7 +326,7 @@ __global__ void score_kernel(const float2* __restrict__ O, const int32_t* __rest
 
 cudaError_t launch_score(const float2* O, const int32_t* Nn, int B, int nq, double* score,
                          cudaStream_t st) {
-    score_kernel<<<B, 256, 0, st>>>(O, Nn, nq, score);
+    ssb_score<<<B, 256, 0, st>>>(O, Nn, nq, score);
     count_launch();
     return cudaGetLastError();
 }

@@ -140,6 +140,15 @@ def test_full_scan_size_small_detector(ssb):
     _check_against_oracle(ssb, frames, g, AB)
 
 
+def test_full_scan_size_float32_frames(ssb):
+    """n = 512 with float32 frames (the general two-pass kernels at this size)."""
+    rng = np.random.default_rng(11)
+    n, det = 512, 8
+    frames = rng.uniform(0, 6, size=(n, n, det, det)).astype(np.float32)
+    g = _geom(n, det, 0.45)
+    _check_against_oracle(ssb, frames, g, AB)
+
+
 def test_max_scan_size_1024(ssb):
     rng = np.random.default_rng(10)
     n, det = 1024, 6
