@@ -111,7 +111,7 @@ static int red_splits(int nq, int n_bf) {
 }
 
 struct WsLayout {
-    size_t tw, xbuf, ktab, chik, amask, Opart, Npart, dcpart, Y, total;
+    size_t tw, xbuf, ktab, chik, Opart, Npart, dcpart, Y, total;
 };
 
 static WsLayout layout(const ssb_geometry* g, int n_bf, int op, int B, int nq) {
@@ -136,9 +136,7 @@ static WsLayout layout(const ssb_geometry* g, int n_bf, int op, int B, int nq) {
     L.ktab = off;
     off += align256((size_t)n_bf * sizeof(float4));
     L.chik = off;
-    off += align256((size_t)B * n_bf * sizeof(float));
-    L.amask = off;
-    off += align256((size_t)n_bf * sizeof(uint32_t));
+    off += align256((size_t)n_bf * kChiStride * sizeof(float));
     L.Opart = off;
     off += align256((size_t)ns * B * nq * sizeof(float2));
     L.Npart = off;
@@ -173,9 +171,8 @@ static int run_reduction(const void* G_dev, const ssb_geometry* g, const int32_t
     cudaError_t e;
     float4* ktab = at<float4>(ws, Lw.ktab);
     float* chik = at<float>(ws, Lw.chik);
-    uint32_t* amask = at<uint32_t>(ws, Lw.amask);
     if ((e = launch_prep(bf_idx, n_bf, g->det_x, g->det_center_y, g->det_center_x, g->det_pitch_invA, sb,
-                         ktab, chik, amask, st)) != cudaSuccess)
+                         ktab, chik, st)) != cudaSuccess)
         return cuda_fail(e, "prep");
     RedLaunch P{};
     P.G = static_cast<const float2*>(G_dev);
@@ -188,7 +185,9 @@ static int run_reduction(const void* G_dev, const ssb_geometry* g, const int32_t
     P.qlist = qlist;
     P.ktab = ktab;
     P.chik = chik;
-    P.amask = amask;
+    P.shared_tilt = 1;
+    for (int s = 1; s < sb.B; ++s)
+        if (sb.s[s].tx != sb.s[0].tx || sb.s[s].ty != sb.s[0].ty) P.shared_tilt = 0;
     P.Opart = at<float2>(ws, Lw.Opart);
     P.Npart = at<int>(ws, Lw.Npart);
     P.dcpart = at<double>(ws, Lw.dcpart);

@@ -211,20 +211,40 @@ struct SetBatch {
     int B;
 };
 
-// Every operation explicitly rounded so that the value is identical in every
-// kernel that evaluates it (k-only tables, single-set and batched passes).
-__device__ __forceinline__ float chi_turns(const float* c, float vx, float vy) {
+// chi/(2 pi) = sum_i c[i] m_i(v) over 12 monomials of v = (vx, vy):
+//   m = (s, u, p, s vx, s vy, vx (xx - 3 yy), vy (3 xx - yy), s^2, s u, s p,
+//        u^2 - 4 p^2, u p),  xx = vx^2, yy = vy^2, s = xx + yy, u = xx - yy, p = vx vy.
+// Every operation is explicitly rounded and the dot product runs in a fixed
+// order, so chi is bit-identical wherever it is evaluated (k-only tables,
+// single-set and batched passes, monomials shared across sets or not).
+__device__ __forceinline__ void chi_monomials(float vx, float vy, float* m) {
     const float xx = __fmul_rn(vx, vx), yy = __fmul_rn(vy, vy);
     const float s = __fadd_rn(xx, yy), u = __fsub_rn(xx, yy), p = __fmul_rn(vx, vy);
-    float d2 = __fmaf_rn(c[2], p, __fmaf_rn(c[1], u, __fmul_rn(c[0], s)));
-    const float t5 = __fmul_rn(vx, __fmaf_rn(-3.0f, yy, xx));
-    const float t6 = __fmul_rn(vy, __fmaf_rn(3.0f, xx, -yy));
-    float d3 = __fmul_rn(s, __fmaf_rn(c[4], vy, __fmul_rn(c[3], vx)));
-    d3 = __fmaf_rn(c[6], t6, __fmaf_rn(c[5], t5, d3));
-    const float q4 = __fmaf_rn(u, u, __fmul_rn(-4.0f, __fmul_rn(p, p)));
-    float d4 = __fmul_rn(s, __fmaf_rn(c[9], p, __fmaf_rn(c[8], u, __fmul_rn(c[7], s))));
-    d4 = __fmaf_rn(c[11], __fmul_rn(u, p), __fmaf_rn(c[10], q4, d4));
-    return __fadd_rn(__fadd_rn(d2, d3), d4);
+    m[0] = s;
+    m[1] = u;
+    m[2] = p;
+    m[3] = __fmul_rn(s, vx);
+    m[4] = __fmul_rn(s, vy);
+    m[5] = __fmul_rn(vx, __fmaf_rn(-3.0f, yy, xx));
+    m[6] = __fmul_rn(vy, __fmaf_rn(3.0f, xx, -yy));
+    m[7] = __fmul_rn(s, s);
+    m[8] = __fmul_rn(s, u);
+    m[9] = __fmul_rn(s, p);
+    m[10] = __fmaf_rn(u, u, __fmul_rn(-4.0f, __fmul_rn(p, p)));
+    m[11] = __fmul_rn(u, p);
+}
+
+__device__ __forceinline__ float chi_dot(const float* c, const float* m) {
+    float a = __fmul_rn(c[0], m[0]);
+#pragma unroll
+    for (int i = 1; i < 12; ++i) a = __fmaf_rn(c[i], m[i], a);
+    return a;
+}
+
+__device__ __forceinline__ float chi_turns(const float* c, float vx, float vy) {
+    float m[12];
+    chi_monomials(vx, vy, m);
+    return chi_dot(c, m);
 }
 
 // Aperture test, float32 contract: dx = px - tx; dy = py - ty;
@@ -253,23 +273,27 @@ int plane512_clusters();
 cudaError_t launch_build512(const uint16_t* frames, int det_pix, const int32_t* bf_idx, int n_bf,
                             float2* G, const float2* tw, void* xbuf, cudaStream_t st);
 
+// k-only table per bright-field pixel: (float32 kx, float32 ky, aperture
+// bits of the sets as float bits, chi_0(k) in turns); chi_s(k) of every set
+// in chik[k * kChiStride + s]
+constexpr int kChiStride = 8;
+
 struct RedLaunch {
     const float2* G;
     int n, n_bf, nq, nsplit, kps;
     double dq;
     const int32_t* qlist;   // null: identity over the half plane
-    float4* ktab;
-    float* chik;            // [B][n_bf]
-    uint32_t* amask;
+    float4* ktab;           // [n_bf]
+    float* chik;            // [n_bf][kChiStride]
     float2* Opart;          // [nsplit][B][nq]
     int* Npart;             // [nsplit][B][nq]
     double* dcpart;         // [nsplit]
     int want_dc;
+    int shared_tilt;        // every set has the same float32 tilt centre
 };
 
 cudaError_t launch_prep(const int32_t* bf_idx, int n_bf, int det_x, double cy, double cx, double dk,
-                        const SetBatch& sb, float4* ktab, float* chik, uint32_t* amask,
-                        cudaStream_t st);
+                        const SetBatch& sb, float4* ktab, float* chik, cudaStream_t st);
 cudaError_t launch_reduce(const RedLaunch& L, const SetBatch& sb, cudaStream_t st);
 cudaError_t launch_finalize(const float2* Opart, const int* Npart, int nsplit, int B, int nq,
                             float2* O, int32_t* N, cudaStream_t st);

@@ -9,6 +9,10 @@
 // compile-time maximum with a uniform b < B guard); chi(k) and the aperture at
 // k are computed once per call into k-only tables.
 //
+// When all sets share one tilt (the batched-scoring case) the three aperture
+// tests and the monomials of chi(k -/+ q) are computed once per (q, k) and
+// only chi's dot product, the phase and the accumulation run per set.
+//
 // Thread <-> q layout: consecutive lanes own consecutive half-plane entries,
 // so each k step reads G[k][q..q+31] as one coalesced 256-byte segment and the
 // sum over k needs no cross-thread reduction.  The k range is split across
@@ -21,31 +25,33 @@ namespace ssb {
 // ---------------------------------------------------------------------------
 // k-only tables: float32 k, aperture bit per set, chi_s(k) in turns
 // ---------------------------------------------------------------------------
-__global__ void ssb_prep(const int32_t* __restrict__ bf_idx, int n_bf, int det_x, double cy,
-                            double cx, double dk, SetBatch sb, float4* __restrict__ ktab,
-                            float* __restrict__ chik, uint32_t* __restrict__ amask) {
+__global__ void ssb_prep(const int32_t* __restrict__ bf_idx, int n_bf, int det_x, double cy, double cx, double dk,
+                         SetBatch sb, float4* __restrict__ ktab, float* __restrict__ chik) {
     const int k = blockIdx.x * blockDim.x + threadIdx.x;
     if (k >= n_bf) return;
     const int idx = bf_idx[k];
     const int i = idx / det_x, j = idx - i * det_x;
     const float kx = __double2float_rn(__dmul_rn(__dsub_rn((double)j, cx), dk));
     const float ky = __double2float_rn(__dmul_rn(__dsub_rn((double)i, cy), dk));
-    ktab[k] = make_float4(kx, ky, 0.f, 0.f);
     uint32_t bits = 0;
-    for (int s = 0; s < sb.B; ++s) {
-        float vx, vy;
-        const bool a = aperture_f32(kx, ky, sb.s[s].tx, sb.s[s].ty, sb.r2, &vx, &vy);
-        bits |= (a ? 1u : 0u) << s;
-        chik[(size_t)s * n_bf + k] = a ? chi_turns(sb.s[s].c, vx, vy) : 0.f;
+    float chi0 = 0.f;
+    for (int s = 0; s < kChiStride; ++s) {
+        float c = 0.f;
+        if (s < sb.B) {
+            float vx, vy;
+            const bool a = aperture_f32(kx, ky, sb.s[s].tx, sb.s[s].ty, sb.r2, &vx, &vy);
+            bits |= (a ? 1u : 0u) << s;
+            c = a ? chi_turns(sb.s[s].c, vx, vy) : 0.f;
+        }
+        if (s == 0) chi0 = c;
+        chik[(size_t)k * kChiStride + s] = c;
     }
-    amask[k] = bits;
+    ktab[k] = make_float4(kx, ky, __uint_as_float(bits), chi0);
 }
 
 cudaError_t launch_prep(const int32_t* bf_idx, int n_bf, int det_x, double cy, double cx, double dk,
-                        const SetBatch& sb, float4* ktab, float* chik, uint32_t* amask,
-                        cudaStream_t st) {
-    ssb_prep<<<(n_bf + 255) / 256, 256, 0, st>>>(bf_idx, n_bf, det_x, cy, cx, dk, sb, ktab, chik,
-                                                    amask);
+                        const SetBatch& sb, float4* ktab, float* chik, cudaStream_t st) {
+    ssb_prep<<<(n_bf + 255) / 256, 256, 0, st>>>(bf_idx, n_bf, det_x, cy, cx, dk, sb, ktab, chik);
     count_launch();
     return cudaGetLastError();
 }
@@ -54,8 +60,23 @@ cudaError_t launch_prep(const int32_t* bf_idx, int n_bf, int det_x, double cy, d
 // fused reduction
 // ---------------------------------------------------------------------------
 constexpr int kRedThreads = 256;
+constexpr int kRedUnroll = 4;  // k steps whose loads are issued together
 
-template <int MAXB>
+// w(q,k) G(q,k) added to acc: d = chi(k) - chi(k -/+ q) in turns, reduced to
+// [-1/2, 1/2] exactly; T-: w = exp(-2 pi i d), T+: w = -exp(+2 pi i d).
+__device__ __forceinline__ void accumulate(float2& acc, float2 g, float chik, float chiq, bool minus) {
+    const float d = __fsub_rn(chik, chiq);
+    const float r = __fsub_rn(d, rintf(d));
+    float sn, cs;
+    __sincosf(__fmul_rn(6.28318530717958648f, r), &sn, &cs);  // |argument| <= pi
+    const float wr = minus ? cs : -cs, wi = -sn;
+    const float re = __fmaf_rn(g.x, wr, __fmul_rn(-g.y, wi));
+    const float im = __fmaf_rn(g.x, wi, __fmul_rn(g.y, wr));
+    acc.x = __fadd_rn(acc.x, re);
+    acc.y = __fadd_rn(acc.y, im);
+}
+
+template <int MAXB, bool SHARED>
 __global__ void __launch_bounds__(kRedThreads)
 ssb_reduce(RedLaunch P, SetBatch sb) {
     const int qi = blockIdx.x * kRedThreads + threadIdx.x;
@@ -82,36 +103,87 @@ ssb_reduce(RedLaunch P, SetBatch sb) {
     const size_t plane = (size_t)P.n * H;
     const float2* gp = P.G + e;
 
-    for (int k = kb; k < ke; ++k) {
-        const float2 g = valid ? __ldg(gp + (size_t)k * plane) : make_float2(0.f, 0.f);
-        const float4 kk = __ldg(P.ktab + k);
-        const uint32_t am = __ldg(P.amask + k);
-        const float mx = __fsub_rn(kk.x, qx), my = __fsub_rn(kk.y, qy);
-        const float px = __fadd_rn(kk.x, qx), py = __fadd_rn(kk.y, qy);
+    auto step = [&](float2 g, float4 kd, int k) {
+        const uint32_t am = __float_as_uint(kd.z);
+        const float mx = __fsub_rn(kd.x, qx), my = __fsub_rn(kd.y, qy);
+        const float px = __fadd_rn(kd.x, qx), py = __fadd_rn(kd.y, qy);
         if (do_dc) dc += (double)g.x;
-#pragma unroll
-        for (int s = 0; s < MAXB; ++s) {
-            if (s < sb.B && ((am >> s) & 1u)) {
+        if constexpr (SHARED && MAXB == 1) {
+            // one set: no branch, so the unrolled k steps can overlap; the
+            // result is committed only on a single-overlap pixel
+            float mvx, mvy, pvx, pvy;
+            const bool m = aperture_f32(mx, my, sb.s[0].tx, sb.s[0].ty, sb.r2, &mvx, &mvy);
+            const bool p = aperture_f32(px, py, sb.s[0].tx, sb.s[0].ty, sb.r2, &pvx, &pvy);
+            const bool act = (am & 1u) && (m != p);
+            float mono[12];
+            chi_monomials(m ? mvx : pvx, m ? mvy : pvy, mono);
+            float2 t = acc[0];
+            accumulate(t, g, kd.w, chi_dot(sb.s[0].c, mono), m);
+            acc[0].x = act ? t.x : acc[0].x;
+            acc[0].y = act ? t.y : acc[0].y;
+            cnt[0] += act ? 1 : 0;
+        } else if constexpr (SHARED) {
+            // one tilt for all sets: the aperture tests and the monomials of
+            // v are common, only the dot product and the phase are per set
+            if (am & 1u) {
                 float mvx, mvy, pvx, pvy;
-                const bool m = aperture_f32(mx, my, sb.s[s].tx, sb.s[s].ty, sb.r2, &mvx, &mvy);
-                const bool p = aperture_f32(px, py, sb.s[s].tx, sb.s[s].ty, sb.r2, &pvx, &pvy);
+                const bool m = aperture_f32(mx, my, sb.s[0].tx, sb.s[0].ty, sb.r2, &mvx, &mvy);
+                const bool p = aperture_f32(px, py, sb.s[0].tx, sb.s[0].ty, sb.r2, &pvx, &pvy);
                 if (m != p) {
-                    const float vx = m ? mvx : pvx, vy = m ? mvy : pvy;
-                    const float cq = chi_turns(sb.s[s].c, vx, vy);
-                    const float d = __fsub_rn(__ldg(P.chik + (size_t)s * P.n_bf + k), cq);
-                    const float r = __fsub_rn(d, rintf(d));
-                    float sn, cs;
-                    sincospif(__fmul_rn(2.0f, r), &sn, &cs);
-                    // T-: w = (cos, -sin); T+: w = (-cos, -sin)
-                    const float wr = m ? cs : -cs, wi = -sn;
-                    const float re = __fmaf_rn(g.x, wr, __fmul_rn(-g.y, wi));
-                    const float im = __fmaf_rn(g.x, wi, __fmul_rn(g.y, wr));
-                    acc[s].x = __fadd_rn(acc[s].x, re);
-                    acc[s].y = __fadd_rn(acc[s].y, im);
-                    cnt[s] += 1;
+                    float mono[12];
+                    chi_monomials(m ? mvx : pvx, m ? mvy : pvy, mono);
+                    cnt[0] += 1;
+                    {
+                        float ck[MAXB];
+                        const float4* cp = reinterpret_cast<const float4*>(P.chik + (size_t)k * kChiStride);
+#pragma unroll
+                        for (int v4 = 0; v4 < (MAXB + 3) / 4; ++v4) {
+                            const float4 c4 = __ldg(cp + v4);
+                            ck[4 * v4] = c4.x;
+                            if (4 * v4 + 1 < MAXB) ck[4 * v4 + 1] = c4.y;
+                            if (4 * v4 + 2 < MAXB) ck[4 * v4 + 2] = c4.z;
+                            if (4 * v4 + 3 < MAXB) ck[4 * v4 + 3] = c4.w;
+                        }
+#pragma unroll
+                        for (int s = 0; s < MAXB; ++s)
+                            if (s < sb.B) accumulate(acc[s], g, ck[s], chi_dot(sb.s[s].c, mono), m);
+                    }
+                }
+            }
+        } else {
+#pragma unroll
+            for (int s = 0; s < MAXB; ++s) {
+                if (s < sb.B && ((am >> s) & 1u)) {
+                    float mvx, mvy, pvx, pvy;
+                    const bool m = aperture_f32(mx, my, sb.s[s].tx, sb.s[s].ty, sb.r2, &mvx, &mvy);
+                    const bool p = aperture_f32(px, py, sb.s[s].tx, sb.s[s].ty, sb.r2, &pvx, &pvy);
+                    if (m != p) {
+                        const float cq = chi_turns(sb.s[s].c, m ? mvx : pvx, m ? mvy : pvy);
+                        accumulate(acc[s], g, __ldg(P.chik + (size_t)k * kChiStride + s), cq, m);
+                        cnt[s] += 1;
+                    }
                 }
             }
         }
+    };
+
+    int k = kb;
+#pragma unroll 1
+    for (; k + kRedUnroll <= ke; k += kRedUnroll) {
+        float2 g[kRedUnroll];
+        float4 kd[kRedUnroll];
+#pragma unroll
+        for (int u = 0; u < kRedUnroll; ++u) {
+            g[u] = valid ? __ldcs(gp + (size_t)(k + u) * plane) : make_float2(0.f, 0.f);
+            kd[u] = __ldg(P.ktab + k + u);
+        }
+#pragma unroll
+        for (int u = 0; u < kRedUnroll; ++u) step(g[u], kd[u], k + u);
+    }
+#pragma unroll 1
+    for (; k < ke; ++k) {
+        const float2 g = valid ? __ldcs(gp + (size_t)k * plane) : make_float2(0.f, 0.f);
+        step(g, __ldg(P.ktab + k), k);
     }
     if (valid) {
 #pragma unroll
@@ -119,23 +191,31 @@ ssb_reduce(RedLaunch P, SetBatch sb) {
             if (s < sb.B) {
                 const size_t o = ((size_t)split * sb.B + s) * P.nq + qi;
                 P.Opart[o] = acc[s];
-                P.Npart[o] = cnt[s];
+                P.Npart[o] = SHARED ? cnt[0] : cnt[s];
             }
         }
     }
     if (do_dc) P.dcpart[split] = dc;
 }
 
+template <int MAXB>
+static void launch_reduce_b(const RedLaunch& P, const SetBatch& sb, dim3 grid, cudaStream_t st) {
+    if (P.shared_tilt)
+        ssb_reduce<MAXB, true><<<grid, kRedThreads, 0, st>>>(P, sb);
+    else
+        ssb_reduce<MAXB, false><<<grid, kRedThreads, 0, st>>>(P, sb);
+}
+
 cudaError_t launch_reduce(const RedLaunch& P, const SetBatch& sb, cudaStream_t st) {
     dim3 grid((P.nq + kRedThreads - 1) / kRedThreads, P.nsplit);
     if (sb.B == 1)
-        ssb_reduce<1><<<grid, kRedThreads, 0, st>>>(P, sb);
+        launch_reduce_b<1>(P, sb, grid, st);
     else if (sb.B == 2)
-        ssb_reduce<2><<<grid, kRedThreads, 0, st>>>(P, sb);
+        launch_reduce_b<2>(P, sb, grid, st);
     else if (sb.B <= 4)
-        ssb_reduce<4><<<grid, kRedThreads, 0, st>>>(P, sb);
+        launch_reduce_b<4>(P, sb, grid, st);
     else
-        ssb_reduce<8><<<grid, kRedThreads, 0, st>>>(P, sb);
+        launch_reduce_b<8>(P, sb, grid, st);
     count_launch();
     return cudaGetLastError();
 }
