@@ -109,11 +109,32 @@ __device__ __forceinline__ void cluster_sync_relaxed() {
     asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+// mbarrier + bulk-copy (TMA) helpers
+__device__ __forceinline__ void mbar_init(uint32_t mbar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(mbar), "r"(count) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(mbar) : "memory");
+}
+// Bounded wait for phase `parity` of the mbarrier: returns false if the
+// copies did not complete within the limit (the caller records the error).
+__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
+    constexpr int kLimit = 1 << 24;
+    for (int i = 0; i < kLimit; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done) : "r"(mbar), "r"(parity) : "memory");
+        if (done) return true;
+    }
+    return false;
+}
 
 __device__ __forceinline__ void discard_l2_line(const void* p) {
     asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
@@ -151,20 +172,19 @@ constexpr int kMaxClusters = 24;
 constexpr size_t kSlabBytes = (size_t)kPlaneM * kPlanePS * sizeof(float2);
 constexpr size_t kPlaneSmem = (size_t)kTwTotal * sizeof(float2) + kSlabBytes + (size_t)kPlaneM * kStageRS * 2;
 
-// stage the 64 rows r_y = j + 8 m of plane Xk: thread i copies 128-byte line
-// i % 8 of row i / 8 (eight 16-byte cp.async)
-__device__ __forceinline__ void stage_rows(const uint16_t* Xk, uint32_t stage, uint32_t j, int tid) {
-    const int m = tid >> 3, l = tid & 7;
-    const char* src = reinterpret_cast<const char*>(Xk + (size_t)(j + kPlaneC * m) * kPlaneN) + 128 * l;
-    const uint32_t dst = stage + (uint32_t)(m * kStageRS * 2 + 128 * l);
-#pragma unroll
-    for (int c = 0; c < 8; ++c) cp_async16(dst + 16 * c, src + 16 * c);
-    cp_async_commit();
+// stage the 64 rows r_y = j + 8 m of plane Xk (1 KB each) into shared memory
+// with bulk copies issued by one thread, completing on `mbar`
+__device__ __forceinline__ void stage_rows(const uint16_t* Xk, uint32_t stage, uint32_t j, uint32_t mbar) {
+    mbar_expect_tx(mbar, (uint32_t)(kPlaneM * kPlaneN * sizeof(uint16_t)));
+#pragma unroll 4
+    for (int m = 0; m < kPlaneM; ++m)
+        bulk_g2s(stage + (uint32_t)(m * kStageRS * 2), Xk + (size_t)(j + kPlaneC * m) * kPlaneN,
+                 (uint32_t)(kPlaneN * sizeof(uint16_t)), mbar);
 }
 
 __global__ void __launch_bounds__(kPlaneThreads, 1)
 ssb_plane512(const uint16_t* __restrict__ X, int k0, int kc, float2* __restrict__ G, const float2* __restrict__ twg,
-             float2* __restrict__ xch) {
+             float2* __restrict__ xch, int* __restrict__ err) {
     constexpr int N = kPlaneN, H = kPlaneH, PS = kPlanePS;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     float2* tws = reinterpret_cast<float2*>(smem_raw);
@@ -174,8 +194,14 @@ ssb_plane512(const uint16_t* __restrict__ X, int k0, int kc, float2* __restrict_
     const int tid = threadIdx.x;
     const uint32_t j = cluster_rank();
     const int ncl = gridDim.x / kPlaneC;
+    __shared__ __align__(8) unsigned long long mbar_storage;
+    const uint32_t mbar = smem_addr(&mbar_storage);
     int kk = blockIdx.x / kPlaneC;
-    if (kk < kc) stage_rows(X + (size_t)kk * N * N, stage, j, tid);
+    if (tid == 0) {
+        mbar_init(mbar, 1);
+        if (kk < kc) stage_rows(X + (size_t)kk * N * N, stage, j, mbar);
+    }
+    uint32_t parity = 0;
 
     for (int i = tid; i < kTwTotal; i += kPlaneThreads) {
         float2 w = make_float2(1.f, 0.f);
@@ -192,12 +218,14 @@ ssb_plane512(const uint16_t* __restrict__ X, int k0, int kc, float2* __restrict_
         }
         tws[i] = w;
     }
+    __syncthreads();  // mbarrier initialised, twiddles in place
 
 #pragma unroll 1
     for (; kk < kc; kk += ncl) {
-        // this thread's staged line has landed; its global copy is dead: drop it
-        // from L2 without write-back
-        cp_async_wait_all();
+        // the staged rows have landed; their global copies are dead: drop them
+        // from L2 without write-back (thread i takes 128-byte line i)
+        if (!mbar_wait(mbar, parity)) atomicExch(err, 1);  // keep going: peers wait on cluster barriers
+        parity ^= 1u;
         discard_l2_line(reinterpret_cast<const char*>(X + (size_t)kk * N * N + (size_t)(j + kPlaneC * (tid >> 3)) * N) +
                         128 * (tid & 7));
         __syncthreads();
@@ -241,8 +269,6 @@ ssb_plane512(const uint16_t* __restrict__ X, int k0, int kc, float2* __restrict_
             }
         }
         __syncthreads();
-        // the staging buffer is free: fetch the next plane while this one finishes
-        if (kk + ncl < kc) stage_rows(X + (size_t)(kk + ncl) * N * N, stage, j, tid);
         // ---- b. local 64-point column DFTs, times W512^(j k_lo), to the L2 exchange ----
         // Thread (t, c): lanes span 32 consecutive columns, t = warp / 2 picks
         // the 8-point sub-sequence; the 8 x 8 transposition goes through the
@@ -303,6 +329,10 @@ ssb_plane512(const uint16_t* __restrict__ X, int k0, int kc, float2* __restrict_
         }
         __syncthreads();
         cluster_sync();  // exchange rows written and visible to the cluster
+        // the staging buffer has been free since the row phase: fetch the next
+        // plane now (issued earlier it competed with the column phase's
+        // exchange stores for the SM's path to L2)
+        if (tid == 0 && kk + ncl < kc) stage_rows(X + (size_t)(kk + ncl) * N * N, stage, j, mbar);
         // ---- c. radix-8 across the cluster, straight to G ----
         {
             float2* Gk = G + (size_t)(k0 + kk) * N * H;
@@ -365,7 +395,7 @@ int plane512_clusters() {
 
 // two gather buffers of 64 planes, then the exchange slots
 size_t plane512_chunk_bytes() {
-    return (size_t)2 * 64 * kPlaneN * kPlaneN * sizeof(uint16_t) + (size_t)kMaxClusters * kXchSlot;
+    return (size_t)2 * 64 * kPlaneN * kPlaneN * sizeof(uint16_t) + (size_t)kMaxClusters * kXchSlot + 256;
 }
 
 // Two internal streams per device (gather, plane) and the events that order
@@ -422,11 +452,13 @@ cudaError_t launch_build512(const uint16_t* frames, int det_pix, const int32_t* 
     const int KC = ncl >= KCMAX ? KCMAX : ncl * (KCMAX / ncl);
     uint16_t* xb[2] = {static_cast<uint16_t*>(xbuf), static_cast<uint16_t*>(xbuf) + (size_t)KCMAX * npos};
     float2* xch = reinterpret_cast<float2*>(static_cast<uint16_t*>(xbuf) + (size_t)2 * KCMAX * npos);
+    int* err = reinterpret_cast<int*>(reinterpret_cast<char*>(xch) + (size_t)kMaxClusters * kXchSlot);
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = kPlaneC;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    if ((e = cudaMemsetAsync(err, 0, sizeof(int), st)) != cudaSuccess) return e;
     // fork from the caller's stream
     if ((e = cudaEventRecord(bs->fork, st)) != cudaSuccess) return e;
     if ((e = cudaStreamWaitEvent(bs->sg, bs->fork, 0)) != cudaSuccess) return e;
@@ -452,7 +484,7 @@ cudaError_t launch_build512(const uint16_t* frames, int det_pix, const int32_t* 
         cfg.stream = bs->sp;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if ((e = cudaLaunchKernelEx(&cfg, ssb_plane512, (const uint16_t*)Xc, k0, kc, G, tw, xch)) != cudaSuccess)
+        if ((e = cudaLaunchKernelEx(&cfg, ssb_plane512, (const uint16_t*)Xc, k0, kc, G, tw, xch, err)) != cudaSuccess)
             return e;
         count_launch();
         if ((e = cudaEventRecord(bs->p_done[b], bs->sp)) != cudaSuccess) return e;
