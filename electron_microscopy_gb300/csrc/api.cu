@@ -142,7 +142,7 @@ static WsLayout layout(const ssb_geometry* g, int n_bf, int op, int B, int nq) {
     L.Npart = off;
     off += align256((size_t)ns * B * nq * sizeof(int));
     L.dcpart = off;
-    off += align256((size_t)ns * sizeof(double));
+    off += align256((size_t)((n_bf + 255) / 256) * sizeof(double));
     if (op == SSB_OP_RECON) {
         L.Y = off;
         off += align256((size_t)n * H * sizeof(float2));
@@ -172,7 +172,8 @@ static int run_reduction(const void* G_dev, const ssb_geometry* g, const int32_t
     float4* ktab = at<float4>(ws, Lw.ktab);
     float* chik = at<float>(ws, Lw.chik);
     if ((e = launch_prep(bf_idx, n_bf, g->det_x, g->det_center_y, g->det_center_x, g->det_pitch_invA, sb,
-                         ktab, chik, st)) != cudaSuccess)
+                         ktab, chik, static_cast<const float2*>(G_dev), (size_t)g->n * (g->n / 2 + 1),
+                         want_dc ? at<double>(ws, Lw.dcpart) : nullptr, st)) != cudaSuccess)
         return cuda_fail(e, "prep");
     RedLaunch P{};
     P.G = static_cast<const float2*>(G_dev);
@@ -190,8 +191,6 @@ static int run_reduction(const void* G_dev, const ssb_geometry* g, const int32_t
         if (sb.s[s].tx != sb.s[0].tx || sb.s[s].ty != sb.s[0].ty) P.shared_tilt = 0;
     P.Opart = at<float2>(ws, Lw.Opart);
     P.Npart = at<int>(ws, Lw.Npart);
-    P.dcpart = at<double>(ws, Lw.dcpart);
-    P.want_dc = want_dc;
     if ((e = launch_reduce(P, sb, st)) != cudaSuccess) return cuda_fail(e, "reduce");
     if ((e = launch_finalize(P.Opart, P.Npart, P.nsplit, sb.B, nq, O, N, st)) != cudaSuccess)
         return cuda_fail(e, "finalize");
@@ -316,7 +315,7 @@ int ssb_reconstruct(const void* G_dev, const ssb_geometry* geom, const int32_t* 
                             ws, Lw, 1, st)) != SSB_OK)
         return rc;
     if ((e = launch_phase(static_cast<const float2*>(O_dev), N_dev, at<double>(ws, Lw.dcpart),
-                          red_splits(nq, n_bf), n_bf, n, at<float2>(ws, Lw.Y), tw, phase_dev, st)) != cudaSuccess)
+                          (n_bf + 255) / 256, n_bf, n, at<float2>(ws, Lw.Y), tw, phase_dev, st)) != cudaSuccess)
         return cuda_fail(e, "phase");
     g_err[0] = 0;
     return SSB_OK;

@@ -287,13 +287,13 @@ struct RedLaunch {
     float* chik;            // [n_bf][kChiStride]
     float2* Opart;          // [nsplit][B][nq]
     int* Npart;             // [nsplit][B][nq]
-    double* dcpart;         // [nsplit]
-    int want_dc;
     int shared_tilt;        // every set has the same float32 tilt centre
 };
 
+// dcpart (may be null): per-256-pixel-block sums of Re G(0,k) in float64
 cudaError_t launch_prep(const int32_t* bf_idx, int n_bf, int det_x, double cy, double cx, double dk,
-                        const SetBatch& sb, float4* ktab, float* chik, cudaStream_t st);
+                        const SetBatch& sb, float4* ktab, float* chik, const float2* G, size_t plane,
+                        double* dcpart, cudaStream_t st);
 cudaError_t launch_reduce(const RedLaunch& L, const SetBatch& sb, cudaStream_t st);
 cudaError_t launch_finalize(const float2* Opart, const int* Npart, int nsplit, int B, int nq,
                             float2* O, int32_t* N, cudaStream_t st);

@@ -25,9 +25,23 @@ namespace ssb {
 // ---------------------------------------------------------------------------
 // k-only tables: float32 k, aperture bit per set, chi_s(k) in turns
 // ---------------------------------------------------------------------------
-__global__ void ssb_prep(const int32_t* __restrict__ bf_idx, int n_bf, int det_x, double cy, double cx, double dk,
-                         SetBatch sb, float4* __restrict__ ktab, float* __restrict__ chik) {
+__global__ void __launch_bounds__(256)
+ssb_prep(const int32_t* __restrict__ bf_idx, int n_bf, int det_x, double cy, double cx, double dk, SetBatch sb,
+         float4* __restrict__ ktab, float* __restrict__ chik, const float2* __restrict__ G, size_t plane,
+         double* __restrict__ dcpart) {
     const int k = blockIdx.x * blockDim.x + threadIdx.x;
+    if (dcpart) {
+        // sum_k Re G(0, k) for the image offset a: per-block partial in
+        // float64, added in a fixed order by the image kernel
+        __shared__ double red[256];
+        red[threadIdx.x] = k < n_bf ? (double)G[(size_t)k * plane].x : 0.0;
+        __syncthreads();
+        for (int w = 128; w > 0; w >>= 1) {
+            if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+            __syncthreads();
+        }
+        if (threadIdx.x == 0) dcpart[blockIdx.x] = red[0];
+    }
     if (k >= n_bf) return;
     const int idx = bf_idx[k];
     const int i = idx / det_x, j = idx - i * det_x;
@@ -50,8 +64,9 @@ __global__ void ssb_prep(const int32_t* __restrict__ bf_idx, int n_bf, int det_x
 }
 
 cudaError_t launch_prep(const int32_t* bf_idx, int n_bf, int det_x, double cy, double cx, double dk,
-                        const SetBatch& sb, float4* ktab, float* chik, cudaStream_t st) {
-    ssb_prep<<<(n_bf + 255) / 256, 256, 0, st>>>(bf_idx, n_bf, det_x, cy, cx, dk, sb, ktab, chik);
+                        const SetBatch& sb, float4* ktab, float* chik, const float2* G, size_t plane,
+                        double* dcpart, cudaStream_t st) {
+    ssb_prep<<<(n_bf + 255) / 256, 256, 0, st>>>(bf_idx, n_bf, det_x, cy, cx, dk, sb, ktab, chik, G, plane, dcpart);
     count_launch();
     return cudaGetLastError();
 }
@@ -98,8 +113,6 @@ ssb_reduce(RedLaunch P, SetBatch sb) {
         acc[s] = make_float2(0.f, 0.f);
         cnt[s] = 0;
     }
-    double dc = 0.0;
-    const bool do_dc = P.want_dc && valid && e == 0;
     const size_t plane = (size_t)P.n * H;
     const float2* gp = P.G + e;
 
@@ -107,7 +120,6 @@ ssb_reduce(RedLaunch P, SetBatch sb) {
         const uint32_t am = __float_as_uint(kd.z);
         const float mx = __fsub_rn(kd.x, qx), my = __fsub_rn(kd.y, qy);
         const float px = __fadd_rn(kd.x, qx), py = __fadd_rn(kd.y, qy);
-        if (do_dc) dc += (double)g.x;
         if constexpr (SHARED && MAXB == 1) {
             // one set: no branch, so the unrolled k steps can overlap; the
             // result is committed only on a single-overlap pixel
@@ -195,7 +207,6 @@ ssb_reduce(RedLaunch P, SetBatch sb) {
             }
         }
     }
-    if (do_dc) P.dcpart[split] = dc;
 }
 
 template <int MAXB>
@@ -297,7 +308,7 @@ ssb_c2r_cols(const float2* __restrict__ O, const int32_t* __restrict__ Nn, float
 
 template <int N>
 __global__ void __launch_bounds__(kPhaseThreads)
-ssb_c2r_rows(const float2* __restrict__ Y, const double* __restrict__ dcpart, int nsplit, int n_bf,
+ssb_c2r_rows(const float2* __restrict__ Y, const double* __restrict__ dcpart, int ndc, int n_bf,
                 const float2* __restrict__ twg, float* __restrict__ phase) {
     constexpr int L = N / 2;
     constexpr int H = N / 2 + 1;
@@ -308,7 +319,7 @@ ssb_c2r_rows(const float2* __restrict__ Y, const double* __restrict__ dcpart, in
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int m = threadIdx.x; m < N; m += kPhaseThreads) tw[m] = twg[m];
     double dc = 0.0;
-    for (int sp = 0; sp < nsplit; ++sp) dc += dcpart[sp];
+    for (int sp = 0; sp < ndc; ++sp) dc += dcpart[sp];
     const float a = (float)(dc / (double)n_bf / ((double)N * (double)N));
     __syncthreads();
     const int row = blockIdx.x * RPB + warp;
