@@ -149,76 +149,91 @@ __device__ __forceinline__ float2 half_pair(uint32_t u) {
 }
 
 // ---------------------------------------------------------------------------
-// one bright-field pixel's 512 x 512 real-to-complex FFT on an 8-CTA cluster;
+// one bright-field pixel's 512 x 512 real-to-complex FFT on a C-CTA cluster;
 // persistent: cluster c handles chunk planes c, c + nclusters, ...
+//   C = 8:  64 scan rows per CTA, 512 threads, ~137 KB shared: 1 CTA per SM
+//   C = 16: 32 scan rows per CTA, 256 threads, ~106 KB shared: 2 CTAs per SM
+//           (kept as a template form; see plane_cluster_size)
 // ---------------------------------------------------------------------------
 constexpr int kPlaneN = 512;
-constexpr int kPlaneC = 8;                 // CTAs per cluster
-constexpr int kPlaneM = kPlaneN / kPlaneC; // scan rows per CTA
 constexpr int kPlaneH = kPlaneN / 2 + 1;
-constexpr int kPlanePS = 258;              // slab row stride (float2); 258 = 2 mod 16: conflict-free columns
-constexpr int kPlaneThreads = 512;
-// shared memory: split-step twiddles W512^k (k <= 256), row twiddles
-// W256^(t k2) laid out [k2][t], column twiddles W64^(t k2) laid out [k2][t],
-// cross twiddles W512^(j k_lo), then the 64 x PS slab
-constexpr int kTwSplit = 0, kTwRow = 260, kTwCol = kTwRow + 256, kTwCross = kTwCol + 64, kTwTotal = kTwCross + 64;
-// staged uint16 rows of the next plane: row stride 544 (16 words mod 32, so the
-// two half-warps reading adjacent rows hit disjoint banks; 16-byte aligned)
-constexpr int kStageRS = 544;
-// cross-CTA exchange through L2: per cluster slot, [rank][k_lo][kXchRS] float2
-constexpr int kXchRS = 264;  // 32-byte aligned rows
-constexpr size_t kXchSlot = (size_t)kPlaneC * kPlaneM * kXchRS * sizeof(float2);
+constexpr int kPlanePS = 258;   // slab row stride (float2)
+constexpr int kStageRS = 544;   // staged uint16 row stride: 16 words mod 32 (disjoint banks for the two
+                                // half-warps reading adjacent rows), 16-byte aligned
+constexpr int kXchRS = 264;     // exchange row stride (float2), 32-byte aligned rows
 constexpr int kMaxClusters = 24;
-constexpr size_t kSlabBytes = (size_t)kPlaneM * kPlanePS * sizeof(float2);
-constexpr size_t kPlaneSmem = (size_t)kTwTotal * sizeof(float2) + kSlabBytes + (size_t)kPlaneM * kStageRS * 2;
+// cross-CTA exchange through L2: per cluster slot, [rank][k_lo][kXchRS] float2,
+// rank x k_lo = 512 rows whatever the cluster size
+constexpr size_t kXchSlot = (size_t)kPlaneN * kXchRS * sizeof(float2);
 
-// stage the 64 rows r_y = j + 8 m of plane Xk (1 KB each) into shared memory
+template <int C>
+struct PlaneCfg {
+    static constexpr int M = kPlaneN / C;                  // scan rows per CTA (local column DFT length)
+    static constexpr int T = M / 8;                        // column threads: DFT8 over n2, then DFT_T over t
+    static constexpr int THREADS = 64 * T;                 // 64 columns per pass
+    static constexpr int MINB = C == 8 ? 1 : 2;
+    // shared memory: split-step twiddles W512^k (k <= 256), row twiddles
+    // W256^(t k2) as [k2][t], column twiddles W_M^(t k2) as [k2][t], cross
+    // twiddles W512^(j k_lo), the M x PS slab, the staged rows
+    static constexpr int TW_SPLIT = 0, TW_ROW = 260, TW_COL = TW_ROW + 256, TW_X = TW_COL + 8 * T,
+                         TW_TOTAL = TW_X + M;
+    static constexpr size_t SLAB = (size_t)M * kPlanePS * sizeof(float2);
+    static constexpr size_t SMEM = (size_t)TW_TOTAL * sizeof(float2) + SLAB + (size_t)M * kStageRS * 2;
+    static_assert(THREADS == 16 * (M / 2), "two row iterations of THREADS/16 rows");
+};
+
+// stage the M rows r_y = j + C m of plane Xk (1 KB each) into shared memory
 // with bulk copies issued by one thread, completing on `mbar`
+template <int C>
 __device__ __forceinline__ void stage_rows(const uint16_t* Xk, uint32_t stage, uint32_t j, uint32_t mbar) {
-    mbar_expect_tx(mbar, (uint32_t)(kPlaneM * kPlaneN * sizeof(uint16_t)));
+    constexpr int M = PlaneCfg<C>::M;
+    mbar_expect_tx(mbar, (uint32_t)(M * kPlaneN * sizeof(uint16_t)));
 #pragma unroll 4
-    for (int m = 0; m < kPlaneM; ++m)
-        bulk_g2s(stage + (uint32_t)(m * kStageRS * 2), Xk + (size_t)(j + kPlaneC * m) * kPlaneN,
+    for (int m = 0; m < M; ++m)
+        bulk_g2s(stage + (uint32_t)(m * kStageRS * 2), Xk + (size_t)(j + C * m) * kPlaneN,
                  (uint32_t)(kPlaneN * sizeof(uint16_t)), mbar);
 }
 
-__global__ void __launch_bounds__(kPlaneThreads, 1)
+template <int C>
+__global__ void __launch_bounds__(PlaneCfg<C>::THREADS, PlaneCfg<C>::MINB)
 ssb_plane512(const uint16_t* __restrict__ X, int k0, int kc, float2* __restrict__ G, const float2* __restrict__ twg,
              float2* __restrict__ xch, int* __restrict__ err) {
-    constexpr int N = kPlaneN, H = kPlaneH, PS = kPlanePS;
+    using Cfg = PlaneCfg<C>;
+    constexpr int N = kPlaneN, H = kPlaneH, PS = kPlanePS, M = Cfg::M, T = Cfg::T, NT = Cfg::THREADS;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     float2* tws = reinterpret_cast<float2*>(smem_raw);
-    float2* slab = tws + kTwTotal;  // [64][PS]
-    const uint32_t* stg = reinterpret_cast<const uint32_t*>(smem_raw + kTwTotal * sizeof(float2) + kSlabBytes);
+    float2* slab = tws + Cfg::TW_TOTAL;  // [M][PS]
+    const uint32_t* stg = reinterpret_cast<const uint32_t*>(smem_raw + Cfg::TW_TOTAL * sizeof(float2) + Cfg::SLAB);
     const uint32_t stage = smem_addr(stg);
     const int tid = threadIdx.x;
     const uint32_t j = cluster_rank();
-    const int ncl = gridDim.x / kPlaneC;
+    const int ncl = gridDim.x / C;
     __shared__ __align__(8) unsigned long long mbar_storage;
     const uint32_t mbar = smem_addr(&mbar_storage);
-    int kk = blockIdx.x / kPlaneC;
+    int kk = blockIdx.x / C;
     if (tid == 0) {
         mbar_init(mbar, 1);
-        if (kk < kc) stage_rows(X + (size_t)kk * N * N, stage, j, mbar);
+        if (kk < kc) stage_rows<C>(X + (size_t)kk * N * N, stage, j, mbar);
     }
     uint32_t parity = 0;
 
-    for (int i = tid; i < kTwTotal; i += kPlaneThreads) {
+    for (int i = tid; i < Cfg::TW_TOTAL; i += NT) {
         float2 w = make_float2(1.f, 0.f);
-        if (i < kTwRow) {
+        if (i < Cfg::TW_ROW) {
             if (i <= N / 2) w = twg[i];
-        } else if (i < kTwCol) {
-            const int k2 = (i - kTwRow) >> 4, t = (i - kTwRow) & 15;
-            w = twg[2 * t * k2];
-        } else if (i < kTwCross) {
-            const int k2 = (i - kTwCol) >> 3, t = (i - kTwCol) & 7;
-            w = twg[8 * t * k2];
+        } else if (i < Cfg::TW_COL) {
+            const int k2 = (i - Cfg::TW_ROW) >> 4, t = (i - Cfg::TW_ROW) & 15;
+            w = twg[2 * t * k2];  // W256^(t k2)
+        } else if (i < Cfg::TW_X) {
+            const int k2 = (i - Cfg::TW_COL) / T, t = (i - Cfg::TW_COL) % T;
+            w = twg[(N / M) * t * k2];  // W_M^(t k2)
         } else {
-            w = twg[j * (i - kTwCross)];
+            w = twg[j * (i - Cfg::TW_X)];  // W512^(j k_lo)
         }
         tws[i] = w;
     }
     __syncthreads();  // mbarrier initialised, twiddles in place
+    float2* xmine = xch + (size_t)(blockIdx.x / C) * (kXchSlot / sizeof(float2));
 
 #pragma unroll 1
     for (; kk < kc; kk += ncl) {
@@ -226,24 +241,24 @@ ssb_plane512(const uint16_t* __restrict__ X, int k0, int kc, float2* __restrict_
         // from L2 without write-back (thread i takes 128-byte line i)
         if (!mbar_wait(mbar, parity)) atomicExch(err, 1);  // keep going: peers wait on cluster barriers
         parity ^= 1u;
-        discard_l2_line(reinterpret_cast<const char*>(X + (size_t)kk * N * N + (size_t)(j + kPlaneC * (tid >> 3)) * N) +
+        discard_l2_line(reinterpret_cast<const char*>(X + (size_t)kk * N * N + (size_t)(j + C * (tid >> 3)) * N) +
                         128 * (tid & 7));
         __syncthreads();
-        // ---- a. row R2C: 16 threads per row, 32 rows at a time ----
+        // ---- a. row R2C: 16 threads per row, NT/16 rows at a time ----
         {
             const int t = tid & 15, hw = tid >> 4;
             const int lane = tid & 31;
             const int src_lane = (lane & 16) | ((16 - t) & 15);
 #pragma unroll 1
-            for (int it = 0; it < kPlaneM / 32; ++it) {
-                const int m = it * 32 + hw;
+            for (int it = 0; it < 2; ++it) {
+                const int m = it * (NT / 16) + hw;
                 const uint32_t* row = stg + m * (kStageRS / 2);
                 float2 v[16];
 #pragma unroll
                 for (int n2 = 0; n2 < 16; ++n2) v[n2] = half_pair(row[t + 16 * n2]);
                 Dft<16>::run(v);
 #pragma unroll
-                for (int k2 = 1; k2 < 16; ++k2) v[k2] = cmul(v[k2], tws[kTwRow + 16 * k2 + t]);  // W256^(t k2)
+                for (int k2 = 1; k2 < 16; ++k2) v[k2] = cmul(v[k2], tws[Cfg::TW_ROW + 16 * k2 + t]);
                 float2* s = slab + m * PS;
 #pragma unroll
                 for (int k2 = 0; k2 < 16; ++k2) s[k2 * 16 + (t ^ k2)] = v[k2];
@@ -262,69 +277,59 @@ ssb_plane512(const uint16_t* __restrict__ X, int k0, int kc, float2* __restrict_
                     const float2 z = v[k1];
                     const float ax = z.x + pr.x, ay = z.y - pr.y;
                     const float bx = z.x - pr.x, by = z.y + pr.y;
-                    const float2 w = tws[kTwSplit + t + 16 * k1];
+                    const float2 w = tws[Cfg::TW_SPLIT + t + 16 * k1];
                     s[t + 16 * k1] = make_float2(ax + w.x * by + w.y * bx, ay - w.x * bx + w.y * by);
                 }
                 if (t == 0) s[N / 2] = make_float2(2.0f * (v[0].x - v[0].y), 0.0f);
             }
         }
         __syncthreads();
-        // ---- b. local 64-point column DFTs, times W512^(j k_lo), to the L2 exchange ----
-        // Thread (t, c): lanes span 32 consecutive columns, t = warp / 2 picks
-        // the 8-point sub-sequence; the 8 x 8 transposition goes through the
-        // column's own slab rows between block barriers.
-        float2* xmine = xch + (size_t)(blockIdx.x / kPlaneC) * (kXchSlot / sizeof(float2));
+        // ---- b. local M-point column DFTs (DFT8 over rows t + T n2, twiddle,
+        //         DFT_T over t), times W512^(j k_lo), to the L2 exchange ----
         {
-            float2* xout = xmine + (size_t)j * kPlaneM * kXchRS;
+            float2* xout = xmine + (size_t)j * M * kXchRS;
             const int t = tid >> 6, cl = tid & 63;
             float2 wc[8], wx[8];
 #pragma unroll
-            for (int k2 = 0; k2 < 8; ++k2) {
-                wc[k2] = tws[kTwCol + 8 * k2 + t];    // W64^(t k2)
-                wx[k2] = tws[kTwCross + t + 8 * k2];  // W512^(j (t + 8 k2))
-            }
-            auto col_in = [&](int c, float2* v) {
+            for (int k2 = 0; k2 < 8; ++k2) wc[k2] = tws[Cfg::TW_COL + k2 * T + t];  // W_M^(t k2)
 #pragma unroll
-                for (int n2 = 0; n2 < 8; ++n2) v[n2] = slab[(t + 8 * n2) * PS + c];
+            for (int i = 0; i < 8 / T; ++i)
+#pragma unroll
+                for (int k1 = 0; k1 < T; ++k1) wx[i * T + k1] = tws[Cfg::TW_X + (t + T * i) + 8 * k1];
+            auto col = [&](int c, int tt, const float2* wcv, const float2* wxv, auto sync) {
+                float2 v[8];
+#pragma unroll
+                for (int n2 = 0; n2 < 8; ++n2) v[n2] = slab[(tt + T * n2) * PS + c];
                 Dft<8>::run(v);
 #pragma unroll
-                for (int k2 = 1; k2 < 8; ++k2) v[k2] = cmul(v[k2], wc[k2]);
-            };
-            auto col_out = [&](int c, float2* v) {
+                for (int k2 = 1; k2 < 8; ++k2) v[k2] = cmul(v[k2], wcv[k2]);
+                sync();
 #pragma unroll
-                for (int n1 = 0; n1 < 8; ++n1) v[n1] = slab[(t * 8 + (n1 ^ t)) * PS + c];
-                Dft<8>::run(v);  // v[k1] = Y[t + 8 k1]
+                for (int k2 = 0; k2 < 8; ++k2) slab[(k2 * T + tt) * PS + c] = v[k2];
+                sync();
 #pragma unroll
-                for (int k1 = 0; k1 < 8; ++k1) xout[(t + 8 * k1) * kXchRS + c] = cmul(v[k1], wx[k1]);
+                for (int i = 0; i < 8 / T; ++i) {
+                    const int k2 = tt + T * i;
+                    float2 u[T];
+#pragma unroll
+                    for (int n1 = 0; n1 < T; ++n1) u[n1] = slab[(k2 * T + n1) * PS + c];
+                    Dft<T>::run(u);  // u[k1] = Y[k2 + 8 k1]
+#pragma unroll
+                    for (int k1 = 0; k1 < T; ++k1) xout[(k2 + 8 * k1) * kXchRS + c] = cmul(u[k1], wxv[i * T + k1]);
+                }
             };
 #pragma unroll 1
-            for (int c = cl; c < N / 2; c += 64) {
-                float2 v[8];
-                col_in(c, v);
-                __syncthreads();
+            for (int c = cl; c < N / 2; c += 64) col(c, t, wc, wx, [] { __syncthreads(); });
+            // column q_x = n/2: lanes 0..T-1 of warp 0, t = lane
+            if (tid < T) {
+                float2 wc2[8], wx2[8];
 #pragma unroll
-                for (int k2 = 0; k2 < 8; ++k2) slab[(k2 * 8 + (t ^ k2)) * PS + c] = v[k2];
-                __syncthreads();
-                col_out(c, v);
-            }
-            // column q_x = n/2: lanes 0..7 of warp 0, t = lane
-            if (tid < 8) {
-                const int tt = tid;
-                float2 v[8];
+                for (int k2 = 0; k2 < 8; ++k2) wc2[k2] = tws[Cfg::TW_COL + k2 * T + tid];
 #pragma unroll
-                for (int n2 = 0; n2 < 8; ++n2) v[n2] = slab[(tt + 8 * n2) * PS + N / 2];
-                Dft<8>::run(v);
+                for (int i = 0; i < 8 / T; ++i)
 #pragma unroll
-                for (int k2 = 1; k2 < 8; ++k2) v[k2] = cmul(v[k2], tws[kTwCol + 8 * k2 + tt]);
-#pragma unroll
-                for (int k2 = 0; k2 < 8; ++k2) slab[(k2 * 8 + (tt ^ k2)) * PS + N / 2] = v[k2];
-                __syncwarp(0xFFu);
-#pragma unroll
-                for (int n1 = 0; n1 < 8; ++n1) v[n1] = slab[(tt * 8 + (n1 ^ tt)) * PS + N / 2];
-                Dft<8>::run(v);
-#pragma unroll
-                for (int k1 = 0; k1 < 8; ++k1)
-                    xout[(tt + 8 * k1) * kXchRS + N / 2] = cmul(v[k1], tws[kTwCross + tt + 8 * k1]);
+                    for (int k1 = 0; k1 < T; ++k1) wx2[i * T + k1] = tws[Cfg::TW_X + (tid + T * i) + 8 * k1];
+                col(N / 2, tid, wc2, wx2, [] { __syncwarp((1u << T) - 1u); });
             }
         }
         __syncthreads();
@@ -332,28 +337,30 @@ ssb_plane512(const uint16_t* __restrict__ X, int k0, int kc, float2* __restrict_
         // the staging buffer has been free since the row phase: fetch the next
         // plane now (issued earlier it competed with the column phase's
         // exchange stores for the SM's path to L2)
-        if (tid == 0 && kk + ncl < kc) stage_rows(X + (size_t)(kk + ncl) * N * N, stage, j, mbar);
-        // ---- c. radix-8 across the cluster, straight to G ----
+        if (tid == 0 && kk + ncl < kc) stage_rows<C>(X + (size_t)(kk + ncl) * N * N, stage, j, mbar);
+        // ---- c. radix-C across the cluster, straight to G ----
         {
             float2* Gk = G + (size_t)(k0 + kk) * N * H;
+            constexpr int KL = M / C;  // k_lo values per CTA
             auto pair = [&](int p) {
-                const int kl = 8 * (int)j + p / H, c = p % H;
+                const int kl = KL * (int)j + p / H, c = p % H;
                 const float2* src = xmine + (size_t)kl * kXchRS + c;
-                float2 v[8];
+                float2 v[C];
 #pragma unroll
-                for (int r = 0; r < kPlaneC; ++r) v[r] = __ldcg(src + (size_t)r * kPlaneM * kXchRS);
-                Dft<8>::run(v);
+                for (int r = 0; r < C; ++r) v[r] = __ldcg(src + (size_t)r * M * kXchRS);
+                Dft<C>::run(v);
 #pragma unroll
-                for (int kh = 0; kh < 8; ++kh) __stcs(Gk + (size_t)(kl + 64 * kh) * H + c, v[kh]);
+                for (int kh = 0; kh < C; ++kh) __stcs(Gk + (size_t)(kl + M * kh) * H + c, v[kh]);
             };
-            constexpr int P = 8 * H;                               // 2056 (k_lo, q_x) pairs
-            constexpr int PFULL = (P / (2 * kPlaneThreads)) * 2 * kPlaneThreads;  // 2048
+            constexpr int P = KL * H;
+            constexpr int PFULL = (P / (2 * NT)) * 2 * NT;
 #pragma unroll 1
-            for (int p = tid; p < PFULL; p += 2 * kPlaneThreads) {
+            for (int p = tid; p < PFULL; p += 2 * NT) {
                 pair(p);
-                pair(p + kPlaneThreads);
+                pair(p + NT);
             }
-            if (PFULL + tid < P) pair(PFULL + tid);
+#pragma unroll 1
+            for (int p = PFULL + tid; p < P; p += NT) pair(p);
         }
         cluster_sync_relaxed();  // every read of this cluster's exchange rows has completed
     }
@@ -362,38 +369,46 @@ ssb_plane512(const uint16_t* __restrict__ X, int k0, int kc, float2* __restrict_
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-
-// co-resident 8-CTA clusters of ssb_plane512 on this device (cached per device)
+// co-resident clusters of ssb_plane512<C> on this device (cached per device)
+template <int C>
 static int plane_clusters() {
     static int cached[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (cached[dev] > 0) return cached[dev];
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kPlaneC;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(kPlaneC, 1, 1);
-    cfg.blockDim = dim3(kPlaneThreads, 1, 1);
-    cfg.dynamicSmemBytes = kPlaneSmem;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    if (cached[dev] != 0) return cached[dev] > 0 ? cached[dev] : 0;
+    using Cfg = PlaneCfg<C>;
     int ncl = 0;
-    if (cudaOccupancyMaxActiveClusters(&ncl, ssb_plane512, &cfg) != cudaSuccess) ncl = 0;
-    cached[dev] = ncl;
+    if (cudaFuncSetAttribute(ssb_plane512<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::SMEM) ==
+            cudaSuccess &&
+        (C <= 8 || cudaFuncSetAttribute(ssb_plane512<C>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+                       cudaSuccess)) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = C;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(C, 1, 1);
+        cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
+        cfg.dynamicSmemBytes = Cfg::SMEM;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&ncl, ssb_plane512<C>, &cfg) != cudaSuccess) ncl = 0;
+    }
+    cudaGetLastError();  // clear a refused attribute or query
+    cached[dev] = ncl > 0 ? ncl : -1;
     return ncl;
 }
 
-int plane512_clusters() {
-    if (cudaFuncSetAttribute(ssb_plane512, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPlaneSmem) !=
-        cudaSuccess)
-        return 0;
-    return plane_clusters();
-}
+// The cluster size used: 8 (portable). 16-CTA clusters (2 CTAs per SM) were
+// measured on GB300: 14 co-resident clusters (112 SMs) against 15 8-CTA
+// clusters (120 SMs), and the same plane throughput (9.32 vs 9.42 ms for all
+// planes of the 512^2 x 9354 workload), so the portable form is kept.
+static int plane_cluster_size() { return plane_clusters<8>() > 0 ? 8 : 0; }
 
-// two gather buffers of 64 planes, then the exchange slots
+int plane512_clusters() { return plane_cluster_size(); }
+
+// two gather buffers of 64 planes, the exchange slots, an error word
 size_t plane512_chunk_bytes() {
     return (size_t)2 * 64 * kPlaneN * kPlaneN * sizeof(uint16_t) + (size_t)kMaxClusters * kXchSlot + 256;
 }
@@ -434,15 +449,14 @@ static cudaError_t get_streams(BuildStreams** out) {
     return cudaSuccess;
 }
 
-cudaError_t launch_build512(const uint16_t* frames, int det_pix, const int32_t* bf_idx, int n_bf, float2* G,
-                            const float2* tw, void* xbuf, cudaStream_t st) {
+template <int C>
+static cudaError_t build512_c(const uint16_t* frames, int det_pix, const int32_t* bf_idx, int n_bf, float2* G,
+                              const float2* tw, void* xbuf, cudaStream_t st) {
+    using Cfg = PlaneCfg<C>;
     constexpr int KCMAX = gather_pixels<uint16_t>();
     const int npos = kPlaneN * kPlaneN;
     cudaError_t e;
-    if ((e = cudaFuncSetAttribute(ssb_plane512, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)kPlaneSmem)) != cudaSuccess)
-        return e;
-    int ncl = plane_clusters();
+    int ncl = plane_clusters<C>();
     if (ncl < 1) return cudaErrorLaunchOutOfResources;
     if (ncl > kMaxClusters) ncl = kMaxClusters;
     BuildStreams* bs = nullptr;
@@ -455,7 +469,7 @@ cudaError_t launch_build512(const uint16_t* frames, int det_pix, const int32_t* 
     int* err = reinterpret_cast<int*>(reinterpret_cast<char*>(xch) + (size_t)kMaxClusters * kXchSlot);
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kPlaneC;
+    attr[0].val.clusterDim.x = C;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     if ((e = cudaMemsetAsync(err, 0, sizeof(int), st)) != cudaSuccess) return e;
@@ -478,13 +492,14 @@ cudaError_t launch_build512(const uint16_t* frames, int det_pix, const int32_t* 
         if ((e = cudaStreamWaitEvent(bs->sp, bs->g_done[b], 0)) != cudaSuccess) return e;
         cudaLaunchConfig_t cfg = {};
         const int grid_cl = kc < ncl ? kc : ncl;
-        cfg.gridDim = dim3(grid_cl * kPlaneC, 1, 1);
-        cfg.blockDim = dim3(kPlaneThreads, 1, 1);
-        cfg.dynamicSmemBytes = kPlaneSmem;
+        cfg.gridDim = dim3(grid_cl * C, 1, 1);
+        cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
+        cfg.dynamicSmemBytes = Cfg::SMEM;
         cfg.stream = bs->sp;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if ((e = cudaLaunchKernelEx(&cfg, ssb_plane512, (const uint16_t*)Xc, k0, kc, G, tw, xch, err)) != cudaSuccess)
+        if ((e = cudaLaunchKernelEx(&cfg, ssb_plane512<C>, (const uint16_t*)Xc, k0, kc, G, tw, xch, err)) !=
+            cudaSuccess)
             return e;
         count_launch();
         if ((e = cudaEventRecord(bs->p_done[b], bs->sp)) != cudaSuccess) return e;
@@ -493,6 +508,12 @@ cudaError_t launch_build512(const uint16_t* frames, int det_pix, const int32_t* 
     // gather through the event chain)
     if ((e = cudaStreamWaitEvent(st, bs->p_done[(c - 1) & 1], 0)) != cudaSuccess) return e;
     return cudaSuccess;
+}
+
+cudaError_t launch_build512(const uint16_t* frames, int det_pix, const int32_t* bf_idx, int n_bf, float2* G,
+                            const float2* tw, void* xbuf, cudaStream_t st) {
+    if (plane_cluster_size() == 8) return build512_c<8>(frames, det_pix, bf_idx, n_bf, G, tw, xbuf, st);
+    return cudaErrorLaunchOutOfResources;
 }
 
 }  // namespace ssb
