@@ -92,7 +92,7 @@ __device__ __forceinline__ void accumulate(float2& acc, float2 g, float chik, fl
 }
 
 template <int MAXB, bool SHARED>
-__global__ void __launch_bounds__(kRedThreads)
+__global__ void __launch_bounds__(kRedThreads, (SHARED && MAXB >= 4) ? 4 : 1)
 ssb_reduce(RedLaunch P, SetBatch sb) {
     const int qi = blockIdx.x * kRedThreads + threadIdx.x;
     const int split = blockIdx.y;
@@ -127,13 +127,17 @@ ssb_reduce(RedLaunch P, SetBatch sb) {
             const bool m = aperture_f32(mx, my, sb.s[0].tx, sb.s[0].ty, sb.r2, &mvx, &mvy);
             const bool p = aperture_f32(px, py, sb.s[0].tx, sb.s[0].ty, sb.r2, &pvx, &pvy);
             const bool act = (am & 1u) && (m != p);
-            float mono[12];
-            chi_monomials(m ? mvx : pvx, m ? mvy : pvy, mono);
-            float2 t = acc[0];
-            accumulate(t, g, kd.w, chi_dot(sb.s[0].c, mono), m);
-            acc[0].x = act ? t.x : acc[0].x;
-            acc[0].y = act ? t.y : acc[0].y;
-            cnt[0] += act ? 1 : 0;
+            // warp-uniform skip: lanes of a warp hold neighbouring q, so whole
+            // warps often have no trotter pixel at this k
+            if (__any_sync(0xffffffffu, act)) {
+                float mono[12];
+                chi_monomials(m ? mvx : pvx, m ? mvy : pvy, mono);
+                float2 t = acc[0];
+                accumulate(t, g, kd.w, chi_dot(sb.s[0].c, mono), m);
+                acc[0].x = act ? t.x : acc[0].x;
+                acc[0].y = act ? t.y : acc[0].y;
+                cnt[0] += act ? 1 : 0;
+            }
         } else if constexpr (SHARED) {
             // one tilt for all sets: the aperture tests and the monomials of
             // v are common, only the dot product and the phase are per set
