@@ -13,21 +13,25 @@
 //     chunk buffer that stays in L2 for the next kernel.
 //  2. ssb_plane512: one cluster of 8 CTAs per bright-field pixel (persistent:
 //     as many clusters as fit, each looping over planes).  CTA j owns scan
-//     rows r_y = j + 8 m (m < 64):
+//     rows r_y = j + 8 m (m < 64), staged from the chunk buffer into shared
+//     memory by 16-byte asynchronous copies issued by every thread:
 //       a. real-to-complex FFT of each of its 64 rows along r_x: a 256-point
 //          complex FFT of the packed even/odd samples (16 threads per row,
 //          two radix-16 passes, one shared-memory transpose) and the split
 //          step, into a 64 x 257 slab in shared memory;
 //       b. for each of the 257 columns, the 64-point DFT over its own rows,
 //          times exp(-2 pi i j k_lo / 512) (8 threads per column, radix 8 x 8);
-//       c. the 64 x 257 results go to an L2-resident exchange slot of the
-//          cluster; cluster barrier; then the last radix-8 stage across the 8
-//          CTAs: CTA j reads the 8 CTAs' entries (k_lo, q_x) for k_lo in
+//       c. the 64 x 257 results go to one of two L2-resident exchange slots
+//          of the cluster; cluster barrier; then the last radix-8 stage across
+//          the 8 CTAs: CTA j reads the 8 CTAs' entries (k_lo, q_x) for k_lo in
 //          [8j, 8j+8) from L2 and writes G[k][k_lo + 64 k_hi][q_x] straight
 //          to HBM, once.  (Reading the slabs through distributed shared
 //          memory instead measured ~34 GB/s per SM, 3x slower than L2.)
-//     The chunk buffer lines it consumed are dropped from L2 without being
-//     written back (discard.global.L2): they are dead.
+//     Phase c of a plane runs during the row phase of the cluster's next
+//     plane (an L2 -> HBM stream under shared-memory arithmetic); the two
+//     exchange slots alternate so that one cluster barrier per plane orders
+//     both.  The chunk buffer lines a CTA consumed are dropped from L2
+//     without being written back (discard.global.L2): they are dead.
 // The HBM traffic of a build is therefore the frames read once plus G
 // written once; the n x (n/2+1) intermediate stays on chip (shared memory
 // and L2).
@@ -109,32 +113,12 @@ __device__ __forceinline__ void cluster_sync_relaxed() {
     asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
 }
 
-// mbarrier + bulk-copy (TMA) helpers
-__device__ __forceinline__ void mbar_init(uint32_t mbar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(mbar), "r"(count) : "memory");
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+// 16-byte asynchronous global -> shared copies (L2 only), and the wait for
+// all of this thread's outstanding ones
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
-__device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 ::"r"(dst), "l"(src), "r"(bytes), "r"(mbar) : "memory");
-}
-// Bounded wait for phase `parity` of the mbarrier: returns false if the
-// copies did not complete within the limit (the caller records the error).
-__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
-    constexpr int kLimit = 1 << 24;
-    for (int i = 0; i < kLimit; ++i) {
-        uint32_t done;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(done) : "r"(mbar), "r"(parity) : "memory");
-        if (done) return true;
-    }
-    return false;
-}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 __device__ __forceinline__ void discard_l2_line(const void* p) {
     asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
@@ -182,22 +166,25 @@ struct PlaneCfg {
     static_assert(THREADS == 16 * (M / 2), "two row iterations of THREADS/16 rows");
 };
 
-// stage the M rows r_y = j + C m of plane Xk (1 KB each) into shared memory
-// with bulk copies issued by one thread, completing on `mbar`
+// stage the M rows r_y = j + C m of plane Xk (1 KB each) into shared memory:
+// every thread issues its share of the 16-byte copies (consecutive threads,
+// consecutive 16 bytes of a row).  Bulk copies of whole rows were measured
+// slower here: the copy engine took ~30 ns per 1 KB row.
 template <int C>
-__device__ __forceinline__ void stage_rows(const uint16_t* Xk, uint32_t stage, uint32_t j, uint32_t mbar) {
-    constexpr int M = PlaneCfg<C>::M;
-    mbar_expect_tx(mbar, (uint32_t)(M * kPlaneN * sizeof(uint16_t)));
-#pragma unroll 4
-    for (int m = 0; m < M; ++m)
-        bulk_g2s(stage + (uint32_t)(m * kStageRS * 2), Xk + (size_t)(j + C * m) * kPlaneN,
-                 (uint32_t)(kPlaneN * sizeof(uint16_t)), mbar);
+__device__ __forceinline__ void stage_rows(const uint16_t* Xk, uint32_t stage, uint32_t j, int tid) {
+    constexpr int M = PlaneCfg<C>::M, NT = PlaneCfg<C>::THREADS;
+    constexpr int CPR = kPlaneN * (int)sizeof(uint16_t) / 16;  // copies per row
+#pragma unroll
+    for (int i = tid; i < M * CPR; i += NT) {
+        const int m = i / CPR, c = i - m * CPR;
+        cp_async16(stage + (uint32_t)(m * kStageRS * 2 + 16 * c), Xk + (size_t)(j + C * m) * kPlaneN + 8 * c);
+    }
 }
 
 template <int C>
 __global__ void __launch_bounds__(PlaneCfg<C>::THREADS, PlaneCfg<C>::MINB)
 ssb_plane512(const uint16_t* __restrict__ X, int k0, int kc, float2* __restrict__ G, const float2* __restrict__ twg,
-             float2* __restrict__ xch, int* __restrict__ err) {
+             float2* __restrict__ xch) {
     using Cfg = PlaneCfg<C>;
     constexpr int N = kPlaneN, H = kPlaneH, PS = kPlanePS, M = Cfg::M, T = Cfg::T, NT = Cfg::THREADS;
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -208,14 +195,8 @@ ssb_plane512(const uint16_t* __restrict__ X, int k0, int kc, float2* __restrict_
     const int tid = threadIdx.x;
     const uint32_t j = cluster_rank();
     const int ncl = gridDim.x / C;
-    __shared__ __align__(8) unsigned long long mbar_storage;
-    const uint32_t mbar = smem_addr(&mbar_storage);
     int kk = blockIdx.x / C;
-    if (tid == 0) {
-        mbar_init(mbar, 1);
-        if (kk < kc) stage_rows<C>(X + (size_t)kk * N * N, stage, j, mbar);
-    }
-    uint32_t parity = 0;
+    if (kk < kc) stage_rows<C>(X + (size_t)kk * N * N, stage, j, tid);
 
     for (int i = tid; i < Cfg::TW_TOTAL; i += NT) {
         float2 w = make_float2(1.f, 0.f);
@@ -232,25 +213,66 @@ ssb_plane512(const uint16_t* __restrict__ X, int k0, int kc, float2* __restrict_
         }
         tws[i] = w;
     }
-    __syncthreads();  // mbarrier initialised, twiddles in place
-    float2* xmine = xch + (size_t)(blockIdx.x / C) * (kXchSlot / sizeof(float2));
+    __syncthreads();  // twiddles in place
+    // two exchange slots per cluster: the column phase of plane i writes slot
+    // i & 1 while the radix-C phase of plane i - 1 still reads the other
+    constexpr size_t kSlotF = kXchSlot / sizeof(float2);
+    float2* xbase = xch + (size_t)(2 * (blockIdx.x / C)) * kSlotF;
+    // ---- c. radix-C across the cluster, straight to G: pair p = (k_lo, q_x)
+    //         of a plane whose exchange rows are complete ----
+    constexpr int KL = M / C;        // k_lo values per CTA
+    constexpr int P = KL * H;        // pairs per CTA
+    constexpr int QF = P / NT;       // rounds every thread takes
+    constexpr int PT = P - QF * NT;  // threads taking one more
+    static_assert(QF >= 2, "two rounds before the row phase");
+    auto c_load = [&](const float2* xs, int p, float2 (&v)[C]) {
+        const int kl = KL * (int)j + p / H, c = p % H;
+        const float2* src = xs + (size_t)kl * kXchRS + c;
+#pragma unroll
+        for (int r = 0; r < C; ++r) v[r] = __ldcg(src + (size_t)r * M * kXchRS);
+    };
+    auto c_store = [&](float2* Gk, int p, float2 (&v)[C]) {
+        const int kl = KL * (int)j + p / H, c = p % H;
+        Dft<C>::run(v);
+#pragma unroll
+        for (int kh = 0; kh < C; ++kh) __stcs(Gk + (size_t)(kl + M * kh) * H + c, v[kh]);
+    };
 
+    // Software pipeline over the planes of this cluster: iteration i runs the
+    // radix-C phase of plane i - 1 (an L2 -> HBM stream) inside the row phase
+    // of plane i (shared-memory arithmetic), so that one hides the other, and
+    // the next plane's staging copies fly while the first rounds of it run.
+    int prev = -1;       // plane whose radix-C phase is pending
+    uint32_t slot = 0;   // exchange slot the next column phase writes
 #pragma unroll 1
     for (; kk < kc; kk += ncl) {
+        const float2* xprev = xbase + (size_t)(slot ^ 1u) * kSlotF;
+        float2* Gprev = G + (size_t)(k0 + (prev >= 0 ? prev : 0)) * N * H;
+        if (prev >= 0) {
+            float2 ca[C], cb[C];
+            c_load(xprev, tid, ca);
+            c_load(xprev, tid + NT, cb);
+            c_store(Gprev, tid, ca);
+            c_store(Gprev, tid + NT, cb);
+        }
         // the staged rows have landed; their global copies are dead: drop them
         // from L2 without write-back (thread i takes 128-byte line i)
-        if (!mbar_wait(mbar, parity)) atomicExch(err, 1);  // keep going: peers wait on cluster barriers
-        parity ^= 1u;
+        cp_async_wait_all();
         discard_l2_line(reinterpret_cast<const char*>(X + (size_t)kk * N * N + (size_t)(j + C * (tid >> 3)) * N) +
                         128 * (tid & 7));
         __syncthreads();
-        // ---- a. row R2C: 16 threads per row, NT/16 rows at a time ----
+        // ---- a. row R2C: 16 threads per row, NT/16 rows at a time; rounds
+        //         2 and 3 of the pending radix-C phase ride along ----
         {
             const int t = tid & 15, hw = tid >> 4;
             const int lane = tid & 31;
             const int src_lane = (lane & 16) | ((16 - t) & 15);
 #pragma unroll 1
             for (int it = 0; it < 2; ++it) {
+                const int q = 2 + it;
+                const bool cq = prev >= 0 && q < QF;
+                float2 cv[C];
+                if (cq) c_load(xprev, tid + q * NT, cv);
                 const int m = it * (NT / 16) + hw;
                 const uint32_t* row = stg + m * (kStageRS / 2);
                 float2 v[16];
@@ -281,13 +303,26 @@ ssb_plane512(const uint16_t* __restrict__ X, int k0, int kc, float2* __restrict_
                     s[t + 16 * k1] = make_float2(ax + w.x * by + w.y * bx, ay - w.x * bx + w.y * by);
                 }
                 if (t == 0) s[N / 2] = make_float2(2.0f * (v[0].x - v[0].y), 0.0f);
+                if (cq) c_store(Gprev, tid + q * NT, cv);
+            }
+            // the remaining rounds of the pending radix-C phase
+#pragma unroll 1
+            for (int q = 4; prev >= 0 && q < QF; ++q) {
+                float2 cv[C];
+                c_load(xprev, tid + q * NT, cv);
+                c_store(Gprev, tid + q * NT, cv);
+            }
+            if (prev >= 0 && tid < PT) {
+                float2 cv[C];
+                c_load(xprev, tid + QF * NT, cv);
+                c_store(Gprev, tid + QF * NT, cv);
             }
         }
         __syncthreads();
         // ---- b. local M-point column DFTs (DFT8 over rows t + T n2, twiddle,
         //         DFT_T over t), times W512^(j k_lo), to the L2 exchange ----
         {
-            float2* xout = xmine + (size_t)j * M * kXchRS;
+            float2* xout = xbase + (size_t)slot * kSlotF + (size_t)j * M * kXchRS;
             const int t = tid >> 6, cl = tid & 63;
             float2 wc[8], wx[8];
 #pragma unroll
@@ -333,36 +368,39 @@ ssb_plane512(const uint16_t* __restrict__ X, int k0, int kc, float2* __restrict_
             }
         }
         __syncthreads();
-        cluster_sync();  // exchange rows written and visible to the cluster
+        // exchange rows of this plane written and visible to the cluster; every
+        // read of the other slot (the previous plane's) has completed, so the
+        // next column phase may overwrite it
+        cluster_sync();
         // the staging buffer has been free since the row phase: fetch the next
         // plane now (issued earlier it competed with the column phase's
         // exchange stores for the SM's path to L2)
-        if (tid == 0 && kk + ncl < kc) stage_rows<C>(X + (size_t)(kk + ncl) * N * N, stage, j, mbar);
-        // ---- c. radix-C across the cluster, straight to G ----
-        {
-            float2* Gk = G + (size_t)(k0 + kk) * N * H;
-            constexpr int KL = M / C;  // k_lo values per CTA
-            auto pair = [&](int p) {
-                const int kl = KL * (int)j + p / H, c = p % H;
-                const float2* src = xmine + (size_t)kl * kXchRS + c;
-                float2 v[C];
-#pragma unroll
-                for (int r = 0; r < C; ++r) v[r] = __ldcg(src + (size_t)r * M * kXchRS);
-                Dft<C>::run(v);
-#pragma unroll
-                for (int kh = 0; kh < C; ++kh) __stcs(Gk + (size_t)(kl + M * kh) * H + c, v[kh]);
-            };
-            constexpr int P = KL * H;
-            constexpr int PFULL = (P / (2 * NT)) * 2 * NT;
+        if (kk + ncl < kc) stage_rows<C>(X + (size_t)(kk + ncl) * N * N, stage, j, tid);
+        prev = kk;
+        slot ^= 1u;
+    }
+    // the last plane's radix-C phase
+    if (prev >= 0) {
+        const float2* xprev = xbase + (size_t)(slot ^ 1u) * kSlotF;
+        float2* Gprev = G + (size_t)(k0 + prev) * N * H;
 #pragma unroll 1
-            for (int p = tid; p < PFULL; p += 2 * NT) {
-                pair(p);
-                pair(p + NT);
-            }
-#pragma unroll 1
-            for (int p = PFULL + tid; p < P; p += NT) pair(p);
+        for (int q = 0; q + 1 < QF; q += 2) {
+            float2 ca[C], cb[C];
+            c_load(xprev, tid + q * NT, ca);
+            c_load(xprev, tid + (q + 1) * NT, cb);
+            c_store(Gprev, tid + q * NT, ca);
+            c_store(Gprev, tid + (q + 1) * NT, cb);
         }
-        cluster_sync_relaxed();  // every read of this cluster's exchange rows has completed
+        if (QF & 1) {
+            float2 cv[C];
+            c_load(xprev, tid + (QF - 1) * NT, cv);
+            c_store(Gprev, tid + (QF - 1) * NT, cv);
+        }
+        if (tid < PT) {
+            float2 cv[C];
+            c_load(xprev, tid + QF * NT, cv);
+            c_store(Gprev, tid + QF * NT, cv);
+        }
     }
 }
 
@@ -408,9 +446,9 @@ static int plane_cluster_size() { return plane_clusters<8>() > 0 ? 8 : 0; }
 
 int plane512_clusters() { return plane_cluster_size(); }
 
-// two gather buffers of 64 planes, the exchange slots, an error word
+// two gather buffers of 64 planes, two exchange slots per cluster
 size_t plane512_chunk_bytes() {
-    return (size_t)2 * 64 * kPlaneN * kPlaneN * sizeof(uint16_t) + (size_t)kMaxClusters * kXchSlot + 256;
+    return (size_t)2 * 64 * kPlaneN * kPlaneN * sizeof(uint16_t) + (size_t)2 * kMaxClusters * kXchSlot;
 }
 
 // Two internal streams per device (gather, plane) and the events that order
@@ -466,13 +504,11 @@ static cudaError_t build512_c(const uint16_t* frames, int det_pix, const int32_t
     const int KC = ncl >= KCMAX ? KCMAX : ncl * (KCMAX / ncl);
     uint16_t* xb[2] = {static_cast<uint16_t*>(xbuf), static_cast<uint16_t*>(xbuf) + (size_t)KCMAX * npos};
     float2* xch = reinterpret_cast<float2*>(static_cast<uint16_t*>(xbuf) + (size_t)2 * KCMAX * npos);
-    int* err = reinterpret_cast<int*>(reinterpret_cast<char*>(xch) + (size_t)kMaxClusters * kXchSlot);
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = C;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    if ((e = cudaMemsetAsync(err, 0, sizeof(int), st)) != cudaSuccess) return e;
     // fork from the caller's stream
     if ((e = cudaEventRecord(bs->fork, st)) != cudaSuccess) return e;
     if ((e = cudaStreamWaitEvent(bs->sg, bs->fork, 0)) != cudaSuccess) return e;
@@ -498,7 +534,7 @@ static cudaError_t build512_c(const uint16_t* frames, int det_pix, const int32_t
         cfg.stream = bs->sp;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if ((e = cudaLaunchKernelEx(&cfg, ssb_plane512<C>, (const uint16_t*)Xc, k0, kc, G, tw, xch, err)) !=
+        if ((e = cudaLaunchKernelEx(&cfg, ssb_plane512<C>, (const uint16_t*)Xc, k0, kc, G, tw, xch)) !=
             cudaSuccess)
             return e;
         count_launch();
