@@ -36,7 +36,7 @@ L2_BYTES = 129 * 1024 * 1024
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--steps", type=int, default=60)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--workload", default="full", choices=["full", "large", "mid", "small", "tiny"])
@@ -398,7 +398,7 @@ def run_ours(args, ws, rank, local, pg):
                    "score_ms": score_ms, "score_GBs": bytes_score / (score_ms * 1e-3) / 1e9,
                    "score_terms": terms, "score_terms_per_s": terms / (score_ms * 1e-3),
                    "max_count": d.get("max_count")},
-        "roofline": {"bound": "hbm", "kernel": "ssb_build_G (row + column passes)", "achieved": achieved,
+        "roofline": {"bound": "hbm", "kernel": "ssb_build_G = ssb_gather + ssb_plane512<8> on two internal streams (one C-ABI call, timed on the caller's stream)", "achieved": achieved,
                      "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
                      "peak_source": peak_src, "algorithmic_bytes": bytes_build},
         "clocks": clk, "gpu_launches": launches, "wall_s_timed": t_wall,

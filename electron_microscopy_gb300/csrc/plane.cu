@@ -238,6 +238,20 @@ ssb_plane512(const uint16_t* __restrict__ X, int k0, int kc, float2* __restrict_
         for (int kh = 0; kh < C; ++kh) __stcs(Gk + (size_t)(kl + M * kh) * H + c, v[kh]);
     };
 
+    // this CTA's k_lo block of every rank in exchange slot xs: once its
+    // radix-C reads are done the lines are dead until the slot is rewritten
+    // two planes later; drop them from L2 without write-back
+    auto discard_block = [&](const float2* xs) {
+        constexpr int LINES = KL * kXchRS * (int)sizeof(float2) / 128;
+        static_assert(KL * kXchRS * sizeof(float2) % 128 == 0 && M * kXchRS * sizeof(float2) % 128 == 0,
+                      "exchange blocks are whole 128-byte lines");
+        for (int i = tid; i < C * LINES; i += NT) {
+            const int r = i / LINES, l = i - r * LINES;
+            discard_l2_line(reinterpret_cast<const char*>(xs + (size_t)r * M * kXchRS + (size_t)KL * j * kXchRS) +
+                            128 * l);
+        }
+    };
+
     // Software pipeline over the planes of this cluster: iteration i runs the
     // radix-C phase of plane i - 1 (an L2 -> HBM stream) inside the row phase
     // of plane i (shared-memory arithmetic), so that one hides the other, and
@@ -319,6 +333,7 @@ ssb_plane512(const uint16_t* __restrict__ X, int k0, int kc, float2* __restrict_
             }
         }
         __syncthreads();
+        if (prev >= 0) discard_block(xprev);
         // ---- b. local M-point column DFTs (DFT8 over rows t + T n2, twiddle,
         //         DFT_T over t), times W512^(j k_lo), to the L2 exchange ----
         {
@@ -401,6 +416,8 @@ ssb_plane512(const uint16_t* __restrict__ X, int k0, int kc, float2* __restrict_
             c_load(xprev, tid + QF * NT, cv);
             c_store(Gprev, tid + QF * NT, cv);
         }
+        __syncthreads();
+        discard_block(xprev);
     }
 }
 
