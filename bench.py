@@ -381,6 +381,24 @@ def run_ours(args, ws, rank, local, pg):
                          f"{info['sample_seconds']:.1f} s of CPU work",
                "build_ms": info["build_ms"], "recon_ms": info["recon_ms"], "score_ms": info["score_ms"]}
 
+    # the other stages against their binding units: the reconstruction streams
+    # all of G (HBM); the 8-set scoring pass does one sincos (2 transcendental
+    # ops) per active term, against the XU rate of 16 results per clock per SM
+    # at the median SM clock sampled under load
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    clk_mhz = (clk or {}).get("sm_mhz") or 2070.0
+    xu_peak = 16.0 * sms * clk_mhz * 1e6
+    xu_ach = 2.0 * terms / (score_ms * 1e-3)
+    stage_rooflines = {
+        "reconstruct": {"bound": "hbm", "achieved": bytes_recon / (recon_ms * 1e-3) / 1e9, "peak": hbm,
+                        "unit": "GB/s", "frac": bytes_recon / (recon_ms * 1e-3) / 1e9 / hbm,
+                        "algorithmic_bytes": bytes_recon},
+        "score": {"bound": "xu", "achieved": xu_ach / 1e9, "peak": xu_peak / 1e9, "unit": "Gop/s",
+                  "frac": xu_ach / xu_peak, "ops": 2 * terms,
+                  "peak_source": f"derived: 16 sin/cos per clock per SM x {sms} SMs x {clk_mhz:.0f} MHz",
+                  "hbm_frac": bytes_score / (score_ms * 1e-3) / 1e9 / hbm},
+    }
+
     if rank != 0:
         return 0
     line = {
@@ -398,6 +416,7 @@ def run_ours(args, ws, rank, local, pg):
                    "score_ms": score_ms, "score_GBs": bytes_score / (score_ms * 1e-3) / 1e9,
                    "score_terms": terms, "score_terms_per_s": terms / (score_ms * 1e-3),
                    "max_count": d.get("max_count")},
+        "stage_rooflines": stage_rooflines,
         "roofline": {"bound": "hbm", "kernel": "ssb_build_G = ssb_gather + ssb_plane512<8> on two internal streams (one C-ABI call, timed on the caller's stream)", "achieved": achieved,
                      "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
                      "peak_source": peak_src, "algorithmic_bytes": bytes_build},
