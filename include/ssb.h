@@ -143,6 +143,12 @@ size_t ssb_workspace_bytes(const ssb_geometry* geom, int n_bf, int op, int B, in
  * Source: "Historical WebGPU G(q,k) memory experiment", sections
  * "Implementation" and "Memory planning table" (layout and size
  * n_bf * n * (n/2+1) * 8 bytes).
+ * For n = 512 and uint16 frames the work runs on two library-internal
+ * streams per device (created on the first such call, kept for the process):
+ * they wait on an event recorded on `stream` and `stream` waits on their
+ * last event, so ordering against the caller's stream is as for a single
+ * launch.  Concurrent builds on one device are serialised on the host while
+ * their launches are issued.
  */
 int ssb_build_G(const void* frames, int dtype, const ssb_geometry* geom,
                 const int32_t* bf_idx_dev, int n_bf, void* G_dev,
