@@ -83,6 +83,22 @@ static SetParams set_params(const ssb_geometry* g, const ssb_aberr* a) {
     p.c[9] = (float)(l3 * a->C32b / 2.0);
     p.c[10] = (float)(l3 * a->C34a / 4.0);
     p.c[11] = (float)(l3 * a->C34b);
+    // the quartic-in-vx regrouping, combined in double and rounded once
+    const double d[12] = {lam * a->C10 / 2.0,  lam * a->C12a / 2.0, lam * a->C12b,       l2 * a->C21a / 3.0,
+                          l2 * a->C21b / 3.0,  l2 * a->C23a / 3.0,  l2 * a->C23b / 3.0,  l3 * a->C30 / 4.0,
+                          l3 * a->C32a / 4.0,  l3 * a->C32b / 2.0,  l3 * a->C34a / 4.0,  l3 * a->C34b};
+    p.h[0] = (float)(d[7] + d[8] + d[10]);
+    p.h[1] = (float)(d[3] + d[5]);
+    p.h[2] = (float)(d[9] + d[11]);
+    p.h[3] = (float)(d[0] + d[1]);
+    p.h[4] = (float)(d[4] + 3.0 * d[6]);
+    p.h[5] = (float)(2.0 * d[7] - 6.0 * d[10]);
+    p.h[6] = (float)d[2];
+    p.h[7] = (float)(d[3] - 3.0 * d[5]);
+    p.h[8] = (float)(d[9] - d[11]);
+    p.h[9] = (float)(d[0] - d[1]);
+    p.h[10] = (float)(d[4] - d[6]);
+    p.h[11] = (float)(d[7] - d[8] + d[10]);
     return p;
 }
 

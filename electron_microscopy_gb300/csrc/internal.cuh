@@ -203,6 +203,11 @@ __device__ __forceinline__ void fft_warp(float2* buf, const float2* tw, int lane
 struct SetParams {
     float tx, ty;   // float32(k_t)
     float c[12];
+    // chi/(2 pi) regrouped as a quartic in vx for a fixed vy (see chi_row):
+    // h[0] = c7 + c8 + c10 (the vx^4 coefficient), then the vy-polynomials
+    // of the vx^3..vx^0 coefficients: h1 + h2 y; h3 + h4 y + h5 y^2;
+    // y (h6 + h7 y + h8 y^2); y^2 (h9 + h10 y + h11 y^2)
+    float h[12];
 };
 
 struct SetBatch {
@@ -215,8 +220,10 @@ struct SetBatch {
 //   m = (s, u, p, s vx, s vy, vx (xx - 3 yy), vy (3 xx - yy), s^2, s u, s p,
 //        u^2 - 4 p^2, u p),  xx = vx^2, yy = vy^2, s = xx + yy, u = xx - yy, p = vx vy.
 // Every operation is explicitly rounded and the dot product runs in a fixed
-// order, so chi is bit-identical wherever it is evaluated (k-only tables,
-// single-set and batched passes, monomials shared across sets or not).
+// order, so chi(k) is bit-identical wherever it is evaluated.  The reduction
+// evaluates chi(k -/+ q) through the row form (chi_row, chi_horner below),
+// also in a fixed order, so a set's result does not depend on the batch it
+// runs in.
 __device__ __forceinline__ void chi_monomials(float vx, float vy, float* m) {
     const float xx = __fmul_rn(vx, vx), yy = __fmul_rn(vy, vy);
     const float s = __fadd_rn(xx, yy), u = __fsub_rn(xx, yy), p = __fmul_rn(vx, vy);
@@ -245,6 +252,25 @@ __device__ __forceinline__ float chi_turns(const float* c, float vx, float vy) {
     float m[12];
     chi_monomials(vx, vy, m);
     return chi_dot(c, m);
+}
+
+// Coefficients (a3, a2, a1, a0) of chi(vx, vy)/(2 pi) = (((h0 vx + a3) vx + a2)
+// vx + a1) vx + a0 for one vy: a detector row at one scan frequency has one
+// vy per trotter side, so the reduction evaluates chi(k -/+ q) along the row
+// with 4 FMAs per set instead of the 12-monomial dot product.  Fixed
+// operation order: the values do not depend on where or for which batch this
+// runs.
+__device__ __forceinline__ float4 chi_row(const float* h, float y) {
+    const float yy = __fmul_rn(y, y);
+    const float a3 = __fmaf_rn(h[2], y, h[1]);
+    const float a2 = __fmaf_rn(h[5], yy, __fmaf_rn(h[4], y, h[3]));
+    const float a1 = __fmul_rn(__fmaf_rn(h[8], yy, __fmaf_rn(h[7], y, h[6])), y);
+    const float a0 = __fmul_rn(__fmaf_rn(h[11], yy, __fmaf_rn(h[10], y, h[9])), yy);
+    return make_float4(a3, a2, a1, a0);
+}
+
+__device__ __forceinline__ float chi_horner(float h0, float4 a, float x) {
+    return __fmaf_rn(__fmaf_rn(__fmaf_rn(__fmaf_rn(h0, x, a.x), x, a.y), x, a.z), x, a.w);
 }
 
 // Aperture test, float32 contract: dx = px - tx; dy = py - ty;

@@ -9,15 +9,19 @@
 // compile-time maximum with a uniform b < B guard); chi(k) and the aperture at
 // k are computed once per call into k-only tables.
 //
-// When all sets share one tilt (the batched-scoring case) the three aperture
-// tests and the monomials of chi(k -/+ q) are computed once per (q, k) and
-// only chi's dot product, the phase and the accumulation run per set.
+// chi(k -/+ q) is a quartic in v_x along a detector row (v_y is fixed there
+// for a given q and trotter side): its coefficients are rebuilt once per row
+// and each term costs 4 FMAs per set.  When all sets share one tilt (the
+// batched-scoring case) the three aperture tests are computed once per (q, k)
+// and only the row polynomial, the phase and the accumulation run per set.
 //
 // Thread <-> q layout: consecutive lanes own consecutive half-plane entries,
 // so each k step reads G[k][q..q+31] as one coalesced 256-byte segment and the
 // sum over k needs no cross-thread reduction.  The k range is split across
 // grid.y; partial sums are added in a fixed order by the finalize kernel, so
 // results are deterministic and independent of the number of sets B.
+#include <type_traits>
+
 #include "internal.cuh"
 
 namespace ssb {
@@ -91,8 +95,26 @@ __device__ __forceinline__ void accumulate(float2& acc, float2 g, float chik, fl
     acc.y = __fadd_rn(acc.y, im);
 }
 
+// Row tables of the batched forms: per warp, up to kRowSlots distinct scan
+// rows (q_y) among its 32 lanes (neighbouring entries: normally 1 or 2), per
+// trotter side and set one float4 (a3, a2, a1, a0); the set index is padded
+// to MAXB + 1 so that the (slot, side) groups of one load fall on distinct
+// banks.  A warp whose lanes span more rows evaluates the row form per term.
+constexpr int kRowSlots = 4;
+template <int MAXB>
+__host__ __device__ constexpr int row_tab_stride() { return MAXB + 1; }
+template <int MAXB>
+constexpr size_t red_smem_bytes() {
+    return MAXB > 1 ? (size_t)(kRedThreads / 32) * kRowSlots * 2 * row_tab_stride<MAXB>() * sizeof(float4) : 0;
+}
+
+// resident CTAs per SM the register budget is sized for (the per-set tilt
+// form of the batched pass keeps its per-set aperture state: 2)
 template <int MAXB, bool SHARED>
-__global__ void __launch_bounds__(kRedThreads, (SHARED && MAXB >= 4) ? 4 : 1)
+__host__ __device__ constexpr int red_min_blocks() { return (MAXB == 1 || SHARED) ? 4 : 2; }
+
+template <int MAXB, bool SHARED>
+__global__ void __launch_bounds__(kRedThreads, red_min_blocks<MAXB, SHARED>())
 ssb_reduce(RedLaunch P, SetBatch sb) {
     const int qi = blockIdx.x * kRedThreads + threadIdx.x;
     const int split = blockIdx.y;
@@ -116,7 +138,62 @@ ssb_reduce(RedLaunch P, SetBatch sb) {
     const size_t plane = (size_t)P.n * H;
     const float2* gp = P.G + e;
 
-    auto step = [&](float2 g, float4 kd, int k) {
+    // chi(k -/+ q) along the current detector row: per trotter side and set,
+    // the coefficients of chi as a quartic in vx (vy is fixed along a row at
+    // this q); rebuilt when the k walk enters a new row.  One set: registers;
+    // more: the warp's shared-memory table, indexed by the lane's row slot.
+    extern __shared__ float4 rowtab[];
+    float4 row_m = make_float4(0.f, 0.f, 0.f, 0.f), row_p = row_m;
+    float cur_ky = __int_as_float(0x7fc00000);  // NaN: no row yet
+    const int lane = threadIdx.x & 31;
+    float4* wtab = rowtab + (size_t)(threadIdx.x >> 5) * kRowSlots * 2 * row_tab_stride<MAXB>();
+    int slot = 0, nslots = 1;
+    int lead = 0;  // lanes 0..2*kRowSlots-1: the leading lane of row slot lane/2
+    if constexpr (MAXB > 1) {
+        const int prev_row = __shfl_up_sync(0xffffffffu, row, 1);
+        const unsigned starts = __ballot_sync(0xffffffffu, lane == 0 || row != prev_row);
+        slot = __popc(starts & ((2u << lane) - 1u)) - 1;
+        nslots = __popc(starts);
+        unsigned b = starts;
+        for (int i = 0; i < (lane >> 1) && b; ++i) b &= b - 1u;
+        lead = b ? __ffs(b) - 1 : 0;
+    }
+    const bool row_table = nslots <= kRowSlots;  // warp-uniform
+    auto new_row = [&](float ky) {
+        if constexpr (MAXB == 1) {
+            row_m = chi_row(sb.s[0].h, __fsub_rn(__fsub_rn(ky, qy), sb.s[0].ty));
+            row_p = chi_row(sb.s[0].h, __fsub_rn(__fadd_rn(ky, qy), sb.s[0].ty));
+        } else {
+            // lane 2 i + side fills slot i, trotter side `side` (0: k - q, 1: k + q)
+            const float qs = __shfl_sync(0xffffffffu, qy, lead);
+            __syncwarp();
+            if (row_table && lane < 2 * nslots) {
+                const float kq = (lane & 1) ? __fadd_rn(ky, qs) : __fsub_rn(ky, qs);
+                float4* e = wtab + (size_t)lane * row_tab_stride<MAXB>();
+#pragma unroll
+                for (int s = 0; s < MAXB; ++s)
+                    if (s < sb.B) e[s] = chi_row(sb.s[s].h, __fsub_rn(kq, sb.s[s].ty));
+            }
+            __syncwarp();
+        }
+    };
+    // chi(k -/+ q) of set s at vx = x, vy = y on trotter side m (true: k - q);
+    // TAB: the warp's row table is in use (else the row form per term)
+    auto chi_v = [&](auto tab, int s, bool m, float x, float y) -> float {
+        if constexpr (MAXB == 1) {
+            return chi_horner(sb.s[0].h[0], m ? row_m : row_p, x);
+        } else if constexpr (decltype(tab)::value) {
+            return chi_horner(sb.s[s].h[0], wtab[(size_t)(2 * slot + (m ? 0 : 1)) * row_tab_stride<MAXB>() + s], x);
+        } else {
+            return chi_horner(sb.s[s].h[0], chi_row(sb.s[s].h, y), x);
+        }
+    };
+
+    auto step = [&](float2 g, float4 kd, int k, auto tab) {
+        if (decltype(tab)::value && kd.y != cur_ky) {  // uniform: every lane walks the same k
+            new_row(kd.y);
+            cur_ky = kd.y;
+        }
         const uint32_t am = __float_as_uint(kd.z);
         const float mx = __fsub_rn(kd.x, qx), my = __fsub_rn(kd.y, qy);
         const float px = __fadd_rn(kd.x, qx), py = __fadd_rn(kd.y, qy);
@@ -130,40 +207,35 @@ ssb_reduce(RedLaunch P, SetBatch sb) {
             // warp-uniform skip: lanes of a warp hold neighbouring q, so whole
             // warps often have no trotter pixel at this k
             if (__any_sync(0xffffffffu, act)) {
-                float mono[12];
-                chi_monomials(m ? mvx : pvx, m ? mvy : pvy, mono);
                 float2 t = acc[0];
-                accumulate(t, g, kd.w, chi_dot(sb.s[0].c, mono), m);
+                accumulate(t, g, kd.w, chi_v(tab, 0, m, m ? mvx : pvx, 0.f), m);
                 acc[0].x = act ? t.x : acc[0].x;
                 acc[0].y = act ? t.y : acc[0].y;
                 cnt[0] += act ? 1 : 0;
             }
         } else if constexpr (SHARED) {
-            // one tilt for all sets: the aperture tests and the monomials of
-            // v are common, only the dot product and the phase are per set
+            // one tilt for all sets: the aperture tests are common, only the
+            // row polynomial, the phase and the accumulation run per set
             if (am & 1u) {
                 float mvx, mvy, pvx, pvy;
                 const bool m = aperture_f32(mx, my, sb.s[0].tx, sb.s[0].ty, sb.r2, &mvx, &mvy);
                 const bool p = aperture_f32(px, py, sb.s[0].tx, sb.s[0].ty, sb.r2, &pvx, &pvy);
                 if (m != p) {
-                    float mono[12];
-                    chi_monomials(m ? mvx : pvx, m ? mvy : pvy, mono);
+                    const float x = m ? mvx : pvx, y = m ? mvy : pvy;
                     cnt[0] += 1;
-                    {
-                        float ck[MAXB];
-                        const float4* cp = reinterpret_cast<const float4*>(P.chik + (size_t)k * kChiStride);
+                    float ck[MAXB];
+                    const float4* cp = reinterpret_cast<const float4*>(P.chik + (size_t)k * kChiStride);
 #pragma unroll
-                        for (int v4 = 0; v4 < (MAXB + 3) / 4; ++v4) {
-                            const float4 c4 = __ldg(cp + v4);
-                            ck[4 * v4] = c4.x;
-                            if (4 * v4 + 1 < MAXB) ck[4 * v4 + 1] = c4.y;
-                            if (4 * v4 + 2 < MAXB) ck[4 * v4 + 2] = c4.z;
-                            if (4 * v4 + 3 < MAXB) ck[4 * v4 + 3] = c4.w;
-                        }
-#pragma unroll
-                        for (int s = 0; s < MAXB; ++s)
-                            if (s < sb.B) accumulate(acc[s], g, ck[s], chi_dot(sb.s[s].c, mono), m);
+                    for (int v4 = 0; v4 < (MAXB + 3) / 4; ++v4) {
+                        const float4 c4 = __ldg(cp + v4);
+                        ck[4 * v4] = c4.x;
+                        if (4 * v4 + 1 < MAXB) ck[4 * v4 + 1] = c4.y;
+                        if (4 * v4 + 2 < MAXB) ck[4 * v4 + 2] = c4.z;
+                        if (4 * v4 + 3 < MAXB) ck[4 * v4 + 3] = c4.w;
                     }
+#pragma unroll
+                    for (int s = 0; s < MAXB; ++s)
+                        if (s < sb.B) accumulate(acc[s], g, ck[s], chi_v(tab, s, m, x, y), m);
                 }
             }
         } else {
@@ -174,7 +246,7 @@ ssb_reduce(RedLaunch P, SetBatch sb) {
                     const bool m = aperture_f32(mx, my, sb.s[s].tx, sb.s[s].ty, sb.r2, &mvx, &mvy);
                     const bool p = aperture_f32(px, py, sb.s[s].tx, sb.s[s].ty, sb.r2, &pvx, &pvy);
                     if (m != p) {
-                        const float cq = chi_turns(sb.s[s].c, m ? mvx : pvx, m ? mvy : pvy);
+                        const float cq = chi_v(tab, s, m, m ? mvx : pvx, m ? mvy : pvy);
                         accumulate(acc[s], g, __ldg(P.chik + (size_t)k * kChiStride + s), cq, m);
                         cnt[s] += 1;
                     }
@@ -183,24 +255,30 @@ ssb_reduce(RedLaunch P, SetBatch sb) {
         }
     };
 
-    int k = kb;
+    auto walk = [&](auto tab) {
+        int k = kb;
 #pragma unroll 1
-    for (; k + kRedUnroll <= ke; k += kRedUnroll) {
-        float2 g[kRedUnroll];
-        float4 kd[kRedUnroll];
+        for (; k + kRedUnroll <= ke; k += kRedUnroll) {
+            float2 g[kRedUnroll];
+            float4 kd[kRedUnroll];
 #pragma unroll
-        for (int u = 0; u < kRedUnroll; ++u) {
-            g[u] = valid ? __ldcs(gp + (size_t)(k + u) * plane) : make_float2(0.f, 0.f);
-            kd[u] = __ldg(P.ktab + k + u);
+            for (int u = 0; u < kRedUnroll; ++u) {
+                g[u] = valid ? __ldcs(gp + (size_t)(k + u) * plane) : make_float2(0.f, 0.f);
+                kd[u] = __ldg(P.ktab + k + u);
+            }
+#pragma unroll
+            for (int u = 0; u < kRedUnroll; ++u) step(g[u], kd[u], k + u, tab);
         }
-#pragma unroll
-        for (int u = 0; u < kRedUnroll; ++u) step(g[u], kd[u], k + u);
-    }
 #pragma unroll 1
-    for (; k < ke; ++k) {
-        const float2 g = valid ? __ldcs(gp + (size_t)k * plane) : make_float2(0.f, 0.f);
-        step(g, __ldg(P.ktab + k), k);
-    }
+        for (; k < ke; ++k) {
+            const float2 g = valid ? __ldcs(gp + (size_t)k * plane) : make_float2(0.f, 0.f);
+            step(g, __ldg(P.ktab + k), k, tab);
+        }
+    };
+    if (MAXB == 1 || row_table)
+        walk(std::true_type{});
+    else
+        walk(std::false_type{});
     if (valid) {
 #pragma unroll
         for (int s = 0; s < MAXB; ++s) {
@@ -213,12 +291,25 @@ ssb_reduce(RedLaunch P, SetBatch sb) {
     }
 }
 
+template <int MAXB, bool SHARED>
+static void launch_reduce_bs(const RedLaunch& P, const SetBatch& sb, dim3 grid, cudaStream_t st) {
+    constexpr size_t smem = red_smem_bytes<MAXB>();
+    if (smem > 48 * 1024) {
+        static bool opted = false;  // idempotent attribute; a racing second set is harmless
+        if (!opted) {
+            cudaFuncSetAttribute(ssb_reduce<MAXB, SHARED>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            opted = true;
+        }
+    }
+    ssb_reduce<MAXB, SHARED><<<grid, kRedThreads, smem, st>>>(P, sb);
+}
+
 template <int MAXB>
 static void launch_reduce_b(const RedLaunch& P, const SetBatch& sb, dim3 grid, cudaStream_t st) {
     if (P.shared_tilt)
-        ssb_reduce<MAXB, true><<<grid, kRedThreads, 0, st>>>(P, sb);
+        launch_reduce_bs<MAXB, true>(P, sb, grid, st);
     else
-        ssb_reduce<MAXB, false><<<grid, kRedThreads, 0, st>>>(P, sb);
+        launch_reduce_bs<MAXB, false>(P, sb, grid, st);
 }
 
 cudaError_t launch_reduce(const RedLaunch& P, const SetBatch& sb, cudaStream_t st) {
