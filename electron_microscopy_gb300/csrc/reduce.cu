@@ -82,18 +82,23 @@ constexpr int kRedThreads = 256;
 constexpr int kRedUnroll = 4;  // k steps whose loads are issued together
 
 // w(q,k) G(q,k) added to acc: d = chi(k) - chi(k -/+ q) in turns, reduced to
-// [-1/2, 1/2] exactly; T-: w = exp(-2 pi i d), T+: w = -exp(+2 pi i d).
-__device__ __forceinline__ void accumulate(float2& acc, float2 g, float chik, float chiq, bool minus) {
+// [-1/2, 1/2] exactly.  T-: w = exp(-2 pi i d); T+: w = -exp(+2 pi i d), which
+// is the T- form with G and the angle negated: the caller passes
+// gs = +/-G and tw = +/-2 pi once per (q, k), and every set adds
+// gs exp(-i tw r) with four FMAs.
+__device__ __forceinline__ void accumulate(float2& acc, float2 gs, float chik, float chiq, float tw) {
     const float d = __fsub_rn(chik, chiq);
     const float r = __fsub_rn(d, rintf(d));
     float sn, cs;
-    __sincosf(__fmul_rn(6.28318530717958648f, r), &sn, &cs);  // |argument| <= pi
-    const float wr = minus ? cs : -cs, wi = -sn;
-    const float re = __fmaf_rn(g.x, wr, __fmul_rn(-g.y, wi));
-    const float im = __fmaf_rn(g.x, wi, __fmul_rn(g.y, wr));
-    acc.x = __fadd_rn(acc.x, re);
-    acc.y = __fadd_rn(acc.y, im);
+    __sincosf(__fmul_rn(tw, r), &sn, &cs);  // |argument| <= pi
+    acc.x = __fmaf_rn(gs.y, sn, __fmaf_rn(gs.x, cs, acc.x));
+    acc.y = __fmaf_rn(-gs.x, sn, __fmaf_rn(gs.y, cs, acc.y));
 }
+
+__device__ __forceinline__ float2 side_sign(float2 g, bool minus) {
+    return minus ? g : make_float2(-g.x, -g.y);
+}
+constexpr float kTwoPi = 6.28318530717958648f;
 
 // Row tables of the batched forms: per warp, up to kRowSlots distinct scan
 // rows (q_y) among its 32 lanes (neighbouring entries: normally 1 or 2), per
@@ -207,10 +212,11 @@ ssb_reduce(RedLaunch P, SetBatch sb) {
             // warp-uniform skip: lanes of a warp hold neighbouring q, so whole
             // warps often have no trotter pixel at this k
             if (__any_sync(0xffffffffu, act)) {
-                float2 t = acc[0];
-                accumulate(t, g, kd.w, chi_v(tab, 0, m, m ? mvx : pvx, 0.f), m);
-                acc[0].x = act ? t.x : acc[0].x;
-                acc[0].y = act ? t.y : acc[0].y;
+                // inactive lanes add an exact zero: gs = 0 * G, and every
+                // later term is finite
+                const float sg = act ? (m ? 1.0f : -1.0f) : 0.0f;
+                accumulate(acc[0], make_float2(__fmul_rn(sg, g.x), __fmul_rn(sg, g.y)), kd.w,
+                           chi_v(tab, 0, m, m ? mvx : pvx, 0.f), m ? kTwoPi : -kTwoPi);
                 cnt[0] += act ? 1 : 0;
             }
         } else if constexpr (SHARED) {
@@ -222,6 +228,8 @@ ssb_reduce(RedLaunch P, SetBatch sb) {
                 const bool p = aperture_f32(px, py, sb.s[0].tx, sb.s[0].ty, sb.r2, &pvx, &pvy);
                 if (m != p) {
                     const float x = m ? mvx : pvx, y = m ? mvy : pvy;
+                    const float2 gs = side_sign(g, m);
+                    const float tw = m ? kTwoPi : -kTwoPi;
                     cnt[0] += 1;
                     float ck[MAXB];
                     const float4* cp = reinterpret_cast<const float4*>(P.chik + (size_t)k * kChiStride);
@@ -235,7 +243,7 @@ ssb_reduce(RedLaunch P, SetBatch sb) {
                     }
 #pragma unroll
                     for (int s = 0; s < MAXB; ++s)
-                        if (s < sb.B) accumulate(acc[s], g, ck[s], chi_v(tab, s, m, x, y), m);
+                        if (s < sb.B) accumulate(acc[s], gs, ck[s], chi_v(tab, s, m, x, y), tw);
                 }
             }
         } else {
@@ -247,7 +255,8 @@ ssb_reduce(RedLaunch P, SetBatch sb) {
                     const bool p = aperture_f32(px, py, sb.s[s].tx, sb.s[s].ty, sb.r2, &pvx, &pvy);
                     if (m != p) {
                         const float cq = chi_v(tab, s, m, m ? mvx : pvx, m ? mvy : pvy);
-                        accumulate(acc[s], g, __ldg(P.chik + (size_t)k * kChiStride + s), cq, m);
+                        accumulate(acc[s], side_sign(g, m), __ldg(P.chik + (size_t)k * kChiStride + s), cq,
+                                   m ? kTwoPi : -kTwoPi);
                         cnt[s] += 1;
                     }
                 }
