@@ -164,6 +164,8 @@ struct PlaneCfg {
     static constexpr size_t SLAB = (size_t)M * kPlanePS * sizeof(float2);
     static constexpr size_t SMEM = (size_t)TW_TOTAL * sizeof(float2) + SLAB + (size_t)M * kStageRS * 2;
     static_assert(THREADS == 16 * (M / 2), "two row iterations of THREADS/16 rows");
+    static_assert(M != 64 || (size_t)2 * 64 * 64 * sizeof(float2) <= (size_t)M * kStageRS * 2,
+                  "two column-transpose buffers fit the staging area");
 };
 
 // stage the M rows r_y = j + C m of plane Xk (1 KB each) into shared memory:
@@ -191,6 +193,7 @@ ssb_plane512(const uint16_t* __restrict__ X, int k0, int kc, float2* __restrict_
     float2* tws = reinterpret_cast<float2*>(smem_raw);
     float2* slab = tws + Cfg::TW_TOTAL;  // [M][PS]
     const uint32_t* stg = reinterpret_cast<const uint32_t*>(smem_raw + Cfg::TW_TOTAL * sizeof(float2) + Cfg::SLAB);
+    float2* scratch = reinterpret_cast<float2*>(smem_raw + Cfg::TW_TOTAL * sizeof(float2) + Cfg::SLAB);
     const uint32_t stage = smem_addr(stg);
     const int tid = threadIdx.x;
     const uint32_t j = cluster_rank();
@@ -236,20 +239,6 @@ ssb_plane512(const uint16_t* __restrict__ X, int k0, int kc, float2* __restrict_
         Dft<C>::run(v);
 #pragma unroll
         for (int kh = 0; kh < C; ++kh) __stcs(Gk + (size_t)(kl + M * kh) * H + c, v[kh]);
-    };
-
-    // this CTA's k_lo block of every rank in exchange slot xs: once its
-    // radix-C reads are done the lines are dead until the slot is rewritten
-    // two planes later; drop them from L2 without write-back
-    auto discard_block = [&](const float2* xs) {
-        constexpr int LINES = KL * kXchRS * (int)sizeof(float2) / 128;
-        static_assert(KL * kXchRS * sizeof(float2) % 128 == 0 && M * kXchRS * sizeof(float2) % 128 == 0,
-                      "exchange blocks are whole 128-byte lines");
-        for (int i = tid; i < C * LINES; i += NT) {
-            const int r = i / LINES, l = i - r * LINES;
-            discard_l2_line(reinterpret_cast<const char*>(xs + (size_t)r * M * kXchRS + (size_t)KL * j * kXchRS) +
-                            128 * l);
-        }
     };
 
     // Software pipeline over the planes of this cluster: iteration i runs the
@@ -333,7 +322,6 @@ ssb_plane512(const uint16_t* __restrict__ X, int k0, int kc, float2* __restrict_
             }
         }
         __syncthreads();
-        if (prev >= 0) discard_block(xprev);
         // ---- b. local M-point column DFTs (DFT8 over rows t + T n2, twiddle,
         //         DFT_T over t), times W512^(j k_lo), to the L2 exchange ----
         {
@@ -368,9 +356,32 @@ ssb_plane512(const uint16_t* __restrict__ X, int k0, int kc, float2* __restrict_
                     for (int k1 = 0; k1 < T; ++k1) xout[(k2 + 8 * k1) * kXchRS + c] = cmul(u[k1], wxv[i * T + k1]);
                 }
             };
+            // columns 0..n/2-1, 64 per batch: the transpose between the two
+            // radix-8 stages goes through one of two [64][64] buffers in the
+            // staging area (idle until the next plane's copies), so one block
+            // barrier per batch suffices: buffer b is rewritten two batches on,
+            // after the next batch's barrier
+            static_assert(T == 8, "batched column transpose written for 64-row slabs");
 #pragma unroll 1
-            for (int c = cl; c < N / 2; c += 64) col(c, t, wc, wx, [] { __syncthreads(); });
-            // column q_x = n/2: lanes 0..T-1 of warp 0, t = lane
+            for (int i = 0; i < N / 2 / 64; ++i) {
+                const int c = cl + 64 * i;
+                float2* buf = scratch + (size_t)(i & 1) * 64 * 64;
+                float2 v[8];
+#pragma unroll
+                for (int n2 = 0; n2 < 8; ++n2) v[n2] = slab[(t + 8 * n2) * PS + c];
+                Dft<8>::run(v);
+#pragma unroll
+                for (int k2 = 1; k2 < 8; ++k2) v[k2] = cmul(v[k2], wc[k2]);
+#pragma unroll
+                for (int k2 = 0; k2 < 8; ++k2) buf[(k2 * 8 + t) * 64 + cl] = v[k2];
+                __syncthreads();
+#pragma unroll
+                for (int n1 = 0; n1 < 8; ++n1) v[n1] = buf[(t * 8 + n1) * 64 + cl];
+                Dft<8>::run(v);  // v[k1] = Y[t + 8 k1]
+#pragma unroll
+                for (int k1 = 0; k1 < 8; ++k1) xout[(t + 8 * k1) * kXchRS + c] = cmul(v[k1], wx[k1]);
+            }
+            // column q_x = n/2: lanes 0..T-1 of warp 0, t = lane, in place
             if (tid < T) {
                 float2 wc2[8], wx2[8];
 #pragma unroll
@@ -416,8 +427,6 @@ ssb_plane512(const uint16_t* __restrict__ X, int k0, int kc, float2* __restrict_
             c_load(xprev, tid + QF * NT, cv);
             c_store(Gprev, tid + QF * NT, cv);
         }
-        __syncthreads();
-        discard_block(xprev);
     }
 }
 
