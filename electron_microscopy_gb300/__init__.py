@@ -34,7 +34,7 @@ STATUS_NAMES = {0: "SSB_OK", 1: "SSB_INVALID_ARG", 2: "SSB_UNSUPPORTED",
 
 EXPORTED = ("ssb_bf_indices", "ssb_band_indices", "ssb_workspace_bytes", "ssb_build_G",
             "ssb_reconstruct", "ssb_score_batch", "ssb_last_error", "ssb_launch_count",
-            "ssb_reconstruct_noalloc")
+            "ssb_reconstruct_noalloc", "ssb_build_G_host", "ssb_build_G_host_bytes")
 
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -81,13 +81,16 @@ def load(path: str | None = None):
     lib.ssb_workspace_bytes.argtypes = [G_p, c_int, c_int, c_int, c_int]
     lib.ssb_workspace_bytes.restype = c_size
     lib.ssb_build_G.argtypes = [c_vp, c_int, G_p, c_vp, c_int, c_vp, c_vp, c_size, c_vp]
+    lib.ssb_build_G_host.argtypes = [c_vp, c_int, G_p, c_vp, c_vp, c_int, c_vp, c_vp, c_size, c_vp]
+    lib.ssb_build_G_host_bytes.argtypes = [G_p, c_int, c_vp, c_int]
+    lib.ssb_build_G_host_bytes.restype = c_size
     lib.ssb_reconstruct.argtypes = [c_vp, G_p, c_vp, c_int, A_p, c_vp, c_vp, c_vp, c_vp, c_size, c_vp]
     lib.ssb_score_batch.argtypes = [c_vp, G_p, c_vp, c_int, A_p, c_int, c_vp, c_int, c_vp, c_vp, c_vp,
                                     c_vp, c_size, c_vp]
     lib.ssb_reconstruct_noalloc.argtypes = [c_vp, G_p, c_vp, c_int, A_p, c_vp, c_vp, c_vp, c_vp]
     lib.ssb_last_error.restype = ctypes.c_char_p
     lib.ssb_launch_count.restype = ctypes.c_longlong
-    for fn in ("ssb_bf_indices", "ssb_band_indices", "ssb_build_G", "ssb_reconstruct",
+    for fn in ("ssb_bf_indices", "ssb_band_indices", "ssb_build_G", "ssb_build_G_host", "ssb_reconstruct",
                "ssb_score_batch", "ssb_reconstruct_noalloc"):
         getattr(lib, fn).restype = c_int
     _lib = lib
@@ -207,6 +210,41 @@ def build_G(frames, geom, bf_idx_dev, G=None, ws=None, stream=None):
     _check("ssb_build_G", lib.ssb_build_G(_ptr(frames), _dtype_code(frames), ctypes.byref(g),
                                           _ptr(bf_idx_dev), n_bf, _ptr(G), ws.ptr(),
                                           ws.nbytes, _stream(stream)))
+    return G
+
+
+def build_G_host_bytes(geom, bf_idx_host, dtype) -> int:
+    """Workspace bytes of build_G_host for this host index list (numpy int32)."""
+    bf = np.ascontiguousarray(bf_idx_host, dtype=np.int32)
+    return int(load().ssb_build_G_host_bytes(ctypes.byref(to_geometry(geom)), int(dtype),
+                                             bf.ctypes.data_as(ctypes.c_void_p), int(bf.size)))
+
+
+def build_G_host(frames_host, geom, bf_idx_host, bf_idx_dev, G=None, ws=None, stream=None):
+    """G(q,k) from frames in host memory (a CPU tensor, pinned for full copy
+    speed): only the detector rows holding bright-field pixels are copied.
+    bf_idx_host (numpy int32) and bf_idx_dev hold the same indices.  The copy
+    is asynchronous on `stream`: keep frames_host alive and unchanged until
+    the stream has passed it."""
+    import torch
+    lib = load()
+    g = to_geometry(geom)
+    bf = np.ascontiguousarray(bf_idx_host, dtype=np.int32)
+    n_bf = int(bf.size)
+    if frames_host.is_cuda or not frames_host.is_contiguous():
+        raise ValueError("frames_host must be a contiguous CPU tensor")
+    if not bf_idx_dev.is_cuda or int(bf_idx_dev.numel()) != n_bf:
+        raise ValueError("bf_idx_dev must be a CUDA tensor with the host list's length")
+    dev = bf_idx_dev.device
+    if G is None:
+        G = torch.empty((n_bf, g.n, g.n // 2 + 1), dtype=torch.complex64, device=dev)
+    dt = _dtype_code(frames_host)
+    need = build_G_host_bytes(g, bf, dt)
+    if ws is None:
+        ws = Workspace(need, dev)
+    _check("ssb_build_G_host", lib.ssb_build_G_host(
+        ctypes.c_void_p(int(frames_host.data_ptr())), dt, ctypes.byref(g), bf.ctypes.data_as(ctypes.c_void_p),
+        _ptr(bf_idx_dev), n_bf, _ptr(G), ws.ptr(), ws.nbytes, _stream(stream)))
     return G
 
 

@@ -306,6 +306,70 @@ int ssb_build_G(const void* frames, int dtype, const ssb_geometry* geom, const i
     return SSB_OK;
 }
 
+// ssb_build_G_host: the detector rows holding bright-field pixels, staged
+// in the workspace ahead of the build workspace
+struct HostLayout {
+    int r0 = 0, rows = 0;
+    size_t crop = 0, idx = 0, build = 0, total = 0;
+};
+
+static int host_layout(const ssb_geometry* geom, int dtype, const int32_t* bf_host, int n_bf, HostLayout* H) {
+    int rc;
+    if ((rc = check_geom(geom)) != SSB_OK) return rc;
+    if (dtype != SSB_U16 && dtype != SSB_F32) return fail(SSB_INVALID_ARG, "dtype must be SSB_U16 or SSB_F32");
+    if (!bf_host) return fail(SSB_INVALID_ARG, "bf_idx_host must not be NULL");
+    const long long det_pix = (long long)geom->det_y * geom->det_x;
+    if (n_bf < 1 || n_bf > det_pix) return fail(SSB_INVALID_ARG, "n_bf=%d out of range", n_bf);
+    int lo = geom->det_y, hi = -1;
+    for (int i = 0; i < n_bf; ++i) {
+        const int v = bf_host[i];
+        if (v < 0 || v >= det_pix) return fail(SSB_INVALID_ARG, "bf_idx_host[%d]=%d outside the detector", i, v);
+        const int r = v / geom->det_x;
+        lo = r < lo ? r : lo;
+        hi = r > hi ? r : hi;
+    }
+    ssb_geometry crop = *geom;
+    crop.det_y = hi - lo + 1;
+    const size_t es = dtype == SSB_U16 ? 2 : 4;
+    H->r0 = lo;
+    H->rows = crop.det_y;
+    H->crop = 0;
+    H->idx = align256((size_t)geom->n * geom->n * crop.det_y * geom->det_x * es);
+    H->build = H->idx + align256((size_t)n_bf * sizeof(int32_t));
+    H->total = H->build + layout(&crop, n_bf, SSB_OP_BUILD, 1, 1).total;
+    return SSB_OK;
+}
+
+size_t ssb_build_G_host_bytes(const ssb_geometry* geom, int dtype, const int32_t* bf_idx_host, int n_bf) {
+    HostLayout H;
+    if (host_layout(geom, dtype, bf_idx_host, n_bf, &H) != SSB_OK) return 0;
+    return H.total;
+}
+
+int ssb_build_G_host(const void* frames_host, int dtype, const ssb_geometry* geom, const int32_t* bf_idx_host,
+                     const int32_t* bf_idx_dev, int n_bf, void* G_dev, void* ws, size_t ws_bytes, void* stream) {
+    int rc;
+    HostLayout H;
+    if ((rc = host_layout(geom, dtype, bf_idx_host, n_bf, &H)) != SSB_OK) return rc;
+    if (!frames_host || !bf_idx_dev || !G_dev) return fail(SSB_INVALID_ARG, "frames, bf_idx and G must not be NULL");
+    if ((rc = check_ws(ws, ws_bytes, H.total)) != SSB_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t es = dtype == SSB_U16 ? 2 : 4;
+    const size_t row_bytes = (size_t)geom->det_x * es;
+    cudaError_t e = cudaMemcpy2DAsync(at<char>(ws, H.crop), (size_t)H.rows * row_bytes,
+                                      static_cast<const char*>(frames_host) + (size_t)H.r0 * row_bytes,
+                                      (size_t)geom->det_y * row_bytes, (size_t)H.rows * row_bytes,
+                                      (size_t)geom->n * geom->n, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy of the bright-field rows");
+    int32_t* idx = at<int32_t>(ws, H.idx);
+    if ((e = launch_shift_idx(bf_idx_dev, n_bf, H.r0 * geom->det_x, idx, st)) != cudaSuccess)
+        return cuda_fail(e, "index shift");
+    ssb_geometry crop = *geom;
+    crop.det_y = H.rows;
+    return ssb_build_G(at<char>(ws, H.crop), dtype, &crop, idx, n_bf, G_dev, at<char>(ws, H.build),
+                       ws_bytes - H.build, stream);
+}
+
 int ssb_reconstruct(const void* G_dev, const ssb_geometry* geom, const int32_t* bf_idx_dev, int n_bf,
                     const ssb_aberr* set, void* O_dev, int32_t* N_dev, float* phase_dev, void* ws,
                     size_t ws_bytes, void* stream) {

@@ -41,6 +41,20 @@ cudaError_t launch_twiddles(float2* tw, int n, cudaStream_t st) {
 }
 
 // ---------------------------------------------------------------------------
+// index shift for a detector crop
+// ---------------------------------------------------------------------------
+__global__ void ssb_shift_idx(const int32_t* __restrict__ in, int n, int shift, int32_t* __restrict__ out) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) out[i] = in[i] - shift;
+}
+
+cudaError_t launch_shift_idx(const int32_t* in, int n, int shift, int32_t* out, cudaStream_t st) {
+    ssb_shift_idx<<<(n + 255) / 256, 256, 0, st>>>(in, n, shift, out);
+    count_launch();
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
 // row pass
 // ---------------------------------------------------------------------------
 constexpr int kRowThreads = 256;

@@ -155,6 +155,33 @@ int ssb_build_G(const void* frames, int dtype, const ssb_geometry* geom,
                 void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * G(q,k) build from frames in HOST memory (page-locked for full copy speed).
+ * Only bright-field pixels carry G ("Historical WebGPU G(q,k) memory
+ * experiment", sections "Implementation" and "Gotchas recorded"), so only
+ * the detector rows r0..r1 that hold them cross the host link: r0 and r1 are
+ * the smallest and largest row of bf_idx_host, and one pitched host-to-device
+ * copy on `stream` moves (r1 - r0 + 1) * det_x of the det_y * det_x elements of
+ * every frame into the workspace.  The build then runs as ssb_build_G on those
+ * rows; G_dev is bit-identical to what ssb_build_G gives on device frames.
+ * frames_host: (n, n, det_y, det_x) uint16 or float32, contiguous; it must
+ * stay valid and unmodified until the copy has completed on `stream`.
+ * bf_idx_host, bf_idx_dev: the same n_bf detector indices, host and device
+ * copies.  The workspace must hold ssb_build_G_host_bytes() bytes.
+ * Errors as ssb_build_G, plus SSB_INVALID_ARG for a host index outside the
+ * detector.
+ */
+int ssb_build_G_host(const void* frames_host, int dtype, const ssb_geometry* geom,
+                     const int32_t* bf_idx_host, const int32_t* bf_idx_dev, int n_bf,
+                     void* G_dev, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Workspace bytes ssb_build_G_host needs for this index list (host): the
+ * staged detector rows of every frame, the shifted index list and the build
+ * workspace.  0 on invalid arguments.
+ */
+size_t ssb_build_G_host_bytes(const ssb_geometry* geom, int dtype, const int32_t* bf_idx_host, int n_bf);
+
+/*
  * One reconstruction at one aberration set (set: host pointer).
  * Writes O_dev (complex64 [n][n/2+1]), N_dev (int32 [n][n/2+1]) and phase_dev
  * (float32 [n][n], row = scan_y).  Source: "Historical WebGPU G(q,k) memory

@@ -161,3 +161,44 @@ def test_no_launches_from_failed_checks(lib):
     g = _g(n=100)
     lib.ssb_build_G(FAKE, 0, ctypes.byref(g), FAKE, 10, FAKE, FAKE, 1 << 30, None)
     assert lib.ssb_launch_count() == before
+
+
+def test_build_G_host_bytes(lib):
+    """Workspace of the host-input build: the BF detector rows of every frame,
+    the shifted index list and the build workspace of the cropped detector."""
+    g = C.geometry(C.WORKLOADS["full"])
+    bf = O.bf_indices(g)
+    rows = bf // g.det_x
+    r0, r1 = int(rows.min()), int(rows.max())
+    crop = C.Geometry(**{**g.__dict__, "det_y": r1 - r0 + 1})
+    a256 = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    want = (a256(g.n * g.n * (r1 - r0 + 1) * g.det_x * 2) + a256(len(bf) * 4)
+            + ssb.workspace_bytes(crop, len(bf), ssb.OP_BUILD))
+    assert ssb.build_G_host_bytes(g, bf, ssb.SSB_U16) == want
+    # the full workload's disk spans rows 42..150 of 192: 57 % of the frame bytes cross the link
+    assert (r0, r1) == (42, 150)
+    assert ssb.build_G_host_bytes(g, bf, ssb.SSB_F32) > want
+    assert ssb.build_G_host_bytes(g, np.array([-1], np.int32), ssb.SSB_U16) == 0
+    assert ssb.build_G_host_bytes(g, np.array([g.det_y * g.det_x], np.int32), ssb.SSB_U16) == 0
+    assert ssb.build_G_host_bytes(g, bf, 7) == 0
+
+
+def test_error_codes_build_host(lib):
+    g = _g()
+    big = 1 << 40
+    bf = np.array([5, 30, 100], np.int32)
+    bfp = bf.ctypes.data_as(ctypes.c_void_p)
+    before = lib.ssb_launch_count()
+    rc = lib.ssb_build_G_host(None, 0, ctypes.byref(g), bfp, FAKE, 3, FAKE, FAKE, big, None)
+    assert rc == ssb.SSB_INVALID_ARG and "NULL" in _err(lib)
+    rc = lib.ssb_build_G_host(FAKE, 0, ctypes.byref(g), None, FAKE, 3, FAKE, FAKE, big, None)
+    assert rc == ssb.SSB_INVALID_ARG
+    bad = np.array([5, 24 * 24], np.int32)
+    rc = lib.ssb_build_G_host(FAKE, 0, ctypes.byref(g), bad.ctypes.data_as(ctypes.c_void_p), FAKE, 2, FAKE, FAKE,
+                              big, None)
+    assert rc == ssb.SSB_INVALID_ARG and "outside the detector" in _err(lib)
+    rc = lib.ssb_build_G_host(FAKE, 0, ctypes.byref(g), bfp, FAKE, 3, FAKE, FAKE, 64, None)
+    assert rc == ssb.SSB_WORKSPACE_TOO_SMALL
+    rc = lib.ssb_build_G_host(FAKE, 0, ctypes.byref(_g(n=100)), bfp, FAKE, 3, FAKE, FAKE, big, None)
+    assert rc == ssb.SSB_UNSUPPORTED
+    assert lib.ssb_launch_count() == before

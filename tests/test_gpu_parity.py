@@ -233,3 +233,28 @@ def test_reconstruct_is_deterministic(ssb, small_G):
     b = ssb.reconstruct(G, d["geom"], bfd, d["ab"])
     for x, y in zip(a, b):
         assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("case", ["tiny", "small", "n512"])
+def test_build_G_host_equals_device_build(ssb, case, tiny_dataset, small_dataset):
+    """The host-input build copies only the detector rows holding bright-field
+    pixels; G is bit for bit the device-input build's, and matches the oracle."""
+    if case == "n512":
+        rng = np.random.default_rng(21)
+        frames = rng.poisson(3.0, size=(512, 512, 12, 12)).astype(np.uint16)
+        g, ab = _geom(512, 12, 0.33), AB
+    else:
+        d = tiny_dataset if case == "tiny" else small_dataset
+        frames, g, ab = d["frames"], d["geom"], d["ab"]
+    bf = O.bf_indices(g, ab.tilt_x_rad, ab.tilt_y_rad)
+    rows = bf // g.det_x
+    assert rows.min() > 0 or rows.max() < g.det_y - 1  # the copy really skips rows
+    bfd = _dev(bf)
+    Gd = ssb.build_G(_frames_dev(frames), g, bfd)
+    host = torch.from_numpy(np.ascontiguousarray(frames.view(np.int16) if frames.dtype == np.uint16
+                                                 else frames)).pin_memory()
+    Gh = ssb.build_G_host(host, g, bf, bfd)
+    torch.cuda.synchronize()
+    assert torch.equal(Gh, Gd)
+    if case != "n512":
+        assert rel(Gh.cpu().numpy(), O.build_G(frames, bf)) < TOL
