@@ -9,7 +9,7 @@ One step = one pass of the whole hot path over the full-size synthetic scan
 Prints one JSON line.  `value` is ms per step (device time, inputs resident
 in HBM, max over ranks); `e2e` is the same step through the public API with
 host buffers: the frames stay in pinned host memory and ssb_build_G_host
-copies the detector rows holding bright-field pixels every step; the phase
+copies the bright-field box of every frame each step; the phase
 image and the scores are copied out every step.  `--impl reference` times the CPU float64 oracle on a bounded sample of
 the same workload instead (rank 0 only).
 """
@@ -331,8 +331,8 @@ def run_ours(args, ws, rank, local, pg):
     achieved = bytes_build / (build_ms * 1e-3) / 1e9
 
     # end to end through the public API with host buffers: the frames stay in
-    # pinned host memory and ssb_build_G_host copies the detector rows that
-    # hold bright-field pixels every step; phase image and scores come back
+    # pinned host memory and ssb_build_G_host copies the bright-field box of
+    # every frame each step; phase image and scores come back
     e2e = None
     if not args.no_e2e:
         host = torch.empty(frames.shape, dtype=frames.dtype, pin_memory=True)
@@ -341,8 +341,9 @@ def run_ours(args, ws, rank, local, pg):
         sc_h = torch.empty(sc.shape, dtype=sc.dtype, pin_memory=True)
         code = ssb.SSB_U16 if frames.element_size() == 2 else ssb.SSB_F32
         ws_h = ssb.Workspace(ssb.build_G_host_bytes(geom, bf, code), dev)
-        rows = int(bf.max()) // geom.det_x - int(bf.min()) // geom.det_x + 1
-        h2d = n * n * rows * geom.det_x * frames.element_size()
+        r_bf, c_bf = bf // geom.det_x, bf % geom.det_x
+        box = (int(r_bf.min()), int(r_bf.max()), int(c_bf.min()), int(c_bf.max()))
+        h2d = n * n * (box[1] - box[0] + 1) * (box[3] - box[2] + 1) * frames.element_size()
         E = max(1, args.e2e_steps)
 
         def e2e_step():
@@ -365,8 +366,8 @@ def run_ours(args, ws, rank, local, pg):
         e2e_ms = allmax(pg, ea.elapsed_time(eb) / E, dev)
         e2e = {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": ph_h.numel() * 4 + sc_h.numel() * 8, "steps": E,
-               "call": f"ssb_build_G_host (detector rows {int(bf.min()) // geom.det_x}.."
-                       f"{int(bf.max()) // geom.det_x} of {geom.det_y}) + ssb_reconstruct + ssb_score_batch"}
+               "call": f"ssb_build_G_host (detector box rows {box[0]}..{box[1]}, columns {box[2]}..{box[3]} of "
+                       f"{geom.det_y}x{geom.det_x}) + ssb_reconstruct + ssb_score_batch"}
         del host, ws_h
 
     cpu = None

@@ -41,15 +41,20 @@ cudaError_t launch_twiddles(float2* tw, int n, cudaStream_t st) {
 }
 
 // ---------------------------------------------------------------------------
-// index shift for a detector crop
+// bright-field indices into a detector crop (the host-input build)
 // ---------------------------------------------------------------------------
-__global__ void ssb_shift_idx(const int32_t* __restrict__ in, int n, int shift, int32_t* __restrict__ out) {
+__global__ void ssb_crop_idx(const int32_t* __restrict__ in, int n, int det_x, int r0, int c0, int cols,
+                             int32_t* __restrict__ out) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i < n) out[i] = in[i] - shift;
+    if (i < n) {
+        const int v = in[i], r = v / det_x;
+        out[i] = (r - r0) * cols + (v - r * det_x - c0);
+    }
 }
 
-cudaError_t launch_shift_idx(const int32_t* in, int n, int shift, int32_t* out, cudaStream_t st) {
-    ssb_shift_idx<<<(n + 255) / 256, 256, 0, st>>>(in, n, shift, out);
+cudaError_t launch_crop_idx(const int32_t* in, int n, int det_x, int r0, int c0, int cols, int32_t* out,
+                            cudaStream_t st) {
+    ssb_crop_idx<<<(n + 255) / 256, 256, 0, st>>>(in, n, det_x, r0, c0, cols, out);
     count_launch();
     return cudaGetLastError();
 }

@@ -291,8 +291,10 @@ cudaError_t launch_twiddles(float2* tw, int n, cudaStream_t st);
 cudaError_t launch_build(const void* frames, int dtype, int n, int det_pix,
                          const int32_t* bf_idx, int n_bf, float2* G, const float2* tw,
                          cudaStream_t st);
-// out[i] = in[i] - shift (bright-field indices into a detector crop)
-cudaError_t launch_shift_idx(const int32_t* in, int n, int shift, int32_t* out, cudaStream_t st);
+// bright-field indices into a detector crop: in[i] = r det_x + c ->
+// out[i] = (r - r0) cols + (c - c0)
+cudaError_t launch_crop_idx(const int32_t* in, int n, int det_x, int r0, int c0, int cols, int32_t* out,
+                            cudaStream_t st);
 // n = 512, uint16 frames: gather + cluster FFT (plane.cu); xbuf holds
 // plane512_chunk_bytes(); plane512_clusters() is 0 when the cluster kernel
 // cannot be scheduled on the current device

@@ -158,11 +158,12 @@ int ssb_build_G(const void* frames, int dtype, const ssb_geometry* geom,
  * G(q,k) build from frames in HOST memory (page-locked for full copy speed).
  * Only bright-field pixels carry G ("Historical WebGPU G(q,k) memory
  * experiment", sections "Implementation" and "Gotchas recorded"), so only
- * the detector rows r0..r1 that hold them cross the host link: r0 and r1 are
- * the smallest and largest row of bf_idx_host, and one pitched host-to-device
- * copy on `stream` moves (r1 - r0 + 1) * det_x of the det_y * det_x elements of
- * every frame into the workspace.  The build then runs as ssb_build_G on those
- * rows; G_dev is bit-identical to what ssb_build_G gives on device frames.
+ * their bounding box on the detector crosses the host link: rows r0..r1 and
+ * columns c0..c1 are the extremes of bf_idx_host, and one pitched copy on
+ * `stream` moves that box of every frame into the workspace (a 2D copy of
+ * whole rows when the box spans the detector's width, else a 3D copy).  The
+ * build then runs as ssb_build_G on the GPU machine; G_dev is bit-identical to what
+ * ssb_build_G gives on device frames.
  * frames_host: (n, n, det_y, det_x) uint16 or float32, contiguous; it must
  * stay valid and unmodified until the copy has completed on `stream`.
  * bf_idx_host, bf_idx_dev: the same n_bf detector indices, host and device
@@ -176,8 +177,8 @@ int ssb_build_G_host(const void* frames_host, int dtype, const ssb_geometry* geo
 
 /*
  * Workspace bytes ssb_build_G_host needs for this index list (host): the
- * staged detector rows of every frame, the shifted index list and the build
- * workspace.  0 on invalid arguments.
+ * staged bright-field box of every frame, the remapped index list and the
+ * build workspace.  0 on invalid arguments.
  */
 size_t ssb_build_G_host_bytes(const ssb_geometry* geom, int dtype, const int32_t* bf_idx_host, int n_bf);
 

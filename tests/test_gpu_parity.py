@@ -235,20 +235,28 @@ def test_reconstruct_is_deterministic(ssb, small_G):
         assert torch.equal(x, y)
 
 
-@pytest.mark.parametrize("case", ["tiny", "small", "n512"])
+@pytest.mark.parametrize("case", ["tiny", "small", "n512", "whole"])
 def test_build_G_host_equals_device_build(ssb, case, tiny_dataset, small_dataset):
-    """The host-input build copies only the detector rows holding bright-field
-    pixels; G is bit for bit the device-input build's, and matches the oracle."""
+    """The host-input build copies only the bright-field bounding box of each
+    frame (3D copy; "whole": every pixel is bright field, the 2D path); G is
+    bit for bit the device-input build's, and matches the oracle."""
     if case == "n512":
         rng = np.random.default_rng(21)
         frames = rng.poisson(3.0, size=(512, 512, 12, 12)).astype(np.uint16)
         g, ab = _geom(512, 12, 0.33), AB
+    elif case == "whole":
+        rng = np.random.default_rng(22)
+        frames = rng.poisson(4.0, size=(64, 64, 6, 6)).astype(np.uint16)
+        g, ab = _geom(64, 6, 0.05), C.Aberrations()
     else:
         d = tiny_dataset if case == "tiny" else small_dataset
         frames, g, ab = d["frames"], d["geom"], d["ab"]
     bf = O.bf_indices(g, ab.tilt_x_rad, ab.tilt_y_rad)
-    rows = bf // g.det_x
-    assert rows.min() > 0 or rows.max() < g.det_y - 1  # the copy really skips rows
+    rows, cols = bf // g.det_x, bf % g.det_x
+    if case == "whole":
+        assert len(bf) == g.det_y * g.det_x
+    else:  # the copy really skips rows and columns
+        assert rows.max() - rows.min() + 1 < g.det_y and cols.max() - cols.min() + 1 < g.det_x
     bfd = _dev(bf)
     Gd = ssb.build_G(_frames_dev(frames), g, bfd)
     host = torch.from_numpy(np.ascontiguousarray(frames.view(np.int16) if frames.dtype == np.uint16
