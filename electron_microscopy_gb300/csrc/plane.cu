@@ -409,19 +409,12 @@ ssb_plane512(const uint16_t* __restrict__ X, int k0, int kc, float2* __restrict_
     if (prev >= 0) {
         const float2* xprev = xbase + (size_t)(slot ^ 1u) * kSlotF;
         float2* Gprev = G + (size_t)(k0 + prev) * N * H;
-#pragma unroll 1
-        for (int q = 0; q + 1 < QF; q += 2) {
-            float2 ca[C], cb[C];
-            c_load(xprev, tid + q * NT, ca);
-            c_load(xprev, tid + (q + 1) * NT, cb);
-            c_store(Gprev, tid + q * NT, ca);
-            c_store(Gprev, tid + (q + 1) * NT, cb);
-        }
-        if (QF & 1) {
-            float2 cv[C];
-            c_load(xprev, tid + (QF - 1) * NT, cv);
-            c_store(Gprev, tid + (QF - 1) * NT, cv);
-        }
+        // nothing else is live here: every round's loads go out at once
+        float2 cv4[QF][C];
+#pragma unroll
+        for (int q = 0; q < QF; ++q) c_load(xprev, tid + q * NT, cv4[q]);
+#pragma unroll
+        for (int q = 0; q < QF; ++q) c_store(Gprev, tid + q * NT, cv4[q]);
         if (tid < PT) {
             float2 cv[C];
             c_load(xprev, tid + QF * NT, cv);
