@@ -169,8 +169,68 @@ ssb_col_c2c(float2* __restrict__ G, int k_begin, const float2* __restrict__ twg)
 }
 
 // ---------------------------------------------------------------------------
+// column pass for n = 1024 (in place on G): 1024 = 32 x 32 in registers.
+// CTA = 8 columns of one plane, 32 threads per column; thread t first takes
+// rows t + 32 r2 (r2 < 32): DFT32 over r2 -> A[t][k2], times W1024^(t k2),
+// transposed through shared memory; then thread k2 takes A[r1][k2] (r1 < 32):
+// DFT32 over r1 -> X[k2 + 32 k1].  A warp covers 8 columns x 4 rows, so every
+// global access is four 64-byte row segments; the shared layout
+// [column][k2][t] with strides 1060 and 33 (float2) puts both the stores and
+// the loads of a warp on distinct bank pairs.
+// ---------------------------------------------------------------------------
+constexpr int kC1024Cols = 8;
+constexpr int kC1024Threads = 256;
+constexpr int kC1024RS = 33;    // k2 stride (float2)
+constexpr int kC1024CS = 1060;  // column stride (float2): 8 words mod 32
+constexpr size_t kC1024Smem = (size_t)kC1024Cols * kC1024CS * sizeof(float2);
+
+__global__ void __launch_bounds__(kC1024Threads, 2)
+ssb_col1024(float2* __restrict__ G, int k_begin, const float2* __restrict__ tw) {
+    constexpr int N = 1024, H = N / 2 + 1;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    float2* S = reinterpret_cast<float2*>(smem_raw);
+    const int tid = threadIdx.x;
+    const int c = tid & 7;                           // column within the group
+    const int t = ((tid >> 3) & 3) + 4 * (tid >> 5);  // 0..31
+    const int col = blockIdx.x * kC1024Cols + c;
+    const bool has = col < H;
+    float2* P = G + (size_t)(k_begin + blockIdx.y) * N * H + (has ? col : 0);
+    float2* Sc = S + c * kC1024CS;
+    float2 v[32];
+#pragma unroll
+    for (int r2 = 0; r2 < 32; ++r2) v[r2] = has ? P[(size_t)(t + 32 * r2) * H] : make_float2(0.f, 0.f);
+    Dft<32>::run(v);  // v[k2] = A[t][k2]
+#pragma unroll
+    for (int k2 = 0; k2 < 32; ++k2) {
+        const float2 w = k2 == 0 ? make_float2(1.f, 0.f) : __ldg(tw + ((t * k2) & (N - 1)));
+        Sc[k2 * kC1024RS + t] = k2 == 0 ? v[k2] : cmul(v[k2], w);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r1 = 0; r1 < 32; ++r1) v[r1] = Sc[t * kC1024RS + r1];  // A[r1][k2 = t]
+    Dft<32>::run(v);  // v[k1] = X[t + 32 k1]
+    if (has) {
+#pragma unroll
+        for (int k1 = 0; k1 < 32; ++k1) P[(size_t)(t + 32 * k1) * H] = v[k1];
+    }
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
+// column pass of one chunk of planes: the 32 x 32 register kernel at n = 1024,
+// the shared-memory Stockham kernel otherwise
+template <int N>
+static void launch_col(float2* G, int k_begin, int count, const float2* tw, size_t cs, cudaStream_t st) {
+    if constexpr (N == 1024) {
+        ssb_col1024<<<dim3((N / 2 + 1 + kC1024Cols - 1) / kC1024Cols, count), kC1024Threads, kC1024Smem, st>>>(
+            G, k_begin, tw);
+    } else {
+        constexpr int NG = (N / 2) / col_width<N>();
+        ssb_col_c2c<N><<<dim3(NG, count), kColThreads, cs, st>>>(G, k_begin, tw);
+    }
+}
+
 template <int N, typename T>
 static cudaError_t build_n(const T* frames, int det_pix, const int32_t* bf_idx, int n_bf,
                            float2* G, const float2* tw, cudaStream_t st) {
@@ -182,12 +242,16 @@ static cudaError_t build_n(const T* frames, int det_pix, const int32_t* bf_idx, 
     if ((e = cudaFuncSetAttribute(ssb_col_c2c<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)cs)) != cudaSuccess)
         return e;
+    if constexpr (N == 1024) {
+        if ((e = cudaFuncSetAttribute(ssb_col1024, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)kC1024Smem)) != cudaSuccess)
+            return e;
+    }
     // chunk of BF pixels whose intermediate rows (chunk * n * (n/2+1) * 8 B)
     // stay well inside L2
     const size_t plane = (size_t)N * (N / 2 + 1) * sizeof(float2);
     int chunk = (int)((48u << 20) / plane);
     chunk = chunk < kRowPix ? kRowPix : (chunk / kRowPix) * kRowPix;
-    constexpr int NG = (N / 2) / col_width<N>();
     int prev_b = -1, prev_e = -1;
     for (int kb = 0; kb < n_bf || prev_b >= 0; kb += chunk) {
         if (kb < n_bf) {
@@ -197,14 +261,14 @@ static cudaError_t build_n(const T* frames, int det_pix, const int32_t* bf_idx, 
             count_launch();
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
             if (prev_b >= 0) {
-                ssb_col_c2c<N><<<dim3(NG, prev_e - prev_b), kColThreads, cs, st>>>(G, prev_b, tw);
+                launch_col<N>(G, prev_b, prev_e - prev_b, tw, cs, st);
                 count_launch();
                 if ((e = cudaGetLastError()) != cudaSuccess) return e;
             }
             prev_b = kb;
             prev_e = ke;
         } else {
-            ssb_col_c2c<N><<<dim3(NG, prev_e - prev_b), kColThreads, cs, st>>>(G, prev_b, tw);
+            launch_col<N>(G, prev_b, prev_e - prev_b, tw, cs, st);
             count_launch();
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
             prev_b = -1;

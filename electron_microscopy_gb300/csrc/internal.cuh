@@ -133,6 +133,40 @@ template <> struct Dft<16> {
     }
 };
 
+// cos and sin of 2 pi k / 32, k < 16 (the mathematical values, rounded to
+// float): W32^k = kCos32[k] - i kSin32[k]
+__device__ constexpr float kCos32[16] = {1.0f, 0.98078528040323043f, 0.92387953251128674f, 0.83146961230254524f,
+                                         0.70710678118654752f, 0.55557023301960218f, 0.38268343236508977f,
+                                         0.19509032201612826f, 0.0f, -0.19509032201612826f, -0.38268343236508977f,
+                                         -0.55557023301960218f, -0.70710678118654752f, -0.83146961230254524f,
+                                         -0.92387953251128674f, -0.98078528040323043f};
+__device__ constexpr float kSin32[16] = {0.0f, 0.19509032201612826f, 0.38268343236508977f, 0.55557023301960218f,
+                                         0.70710678118654752f, 0.83146961230254524f, 0.92387953251128674f,
+                                         0.98078528040323043f, 1.0f, 0.98078528040323043f, 0.92387953251128674f,
+                                         0.83146961230254524f, 0.70710678118654752f, 0.55557023301960218f,
+                                         0.38268343236508977f, 0.19509032201612826f};
+
+template <> struct Dft<32> {
+    // 32 = 2 x 16: DFT16 of the even and of the odd samples, then
+    // X[k] = A[k] + W32^k B[k], X[k + 16] = A[k] - W32^k B[k]; natural order
+    static __device__ __forceinline__ void run(float2* v) {
+        float2 a[16], b[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            a[i] = v[2 * i];
+            b[i] = v[2 * i + 1];
+        }
+        Dft<16>::run(a);
+        Dft<16>::run(b);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const float2 t = cmul(b[k], make_float2(kCos32[k], -kSin32[k]));
+            v[k] = cadd(a[k], t);
+            v[k + 16] = csub(a[k], t);
+        }
+    }
+};
+
 // ---------------------------------------------------------------------------
 // warp-level in-place Stockham pass over a row of L points in shared memory.
 // NS: span of the sub-transforms already done; TWS: stride into the
