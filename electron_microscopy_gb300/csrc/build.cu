@@ -18,6 +18,8 @@
 // The host walks the BF pixels in chunks and issues row(c) and column(c-1)
 // back to back so that a chunk's intermediate rows are still in L2 when the
 // column pass reads them.
+#include <type_traits>
+
 #include "internal.cuh"
 
 namespace ssb {
@@ -216,6 +218,105 @@ ssb_col1024(float2* __restrict__ G, int k_begin, const float2* __restrict__ tw) 
 }
 
 // ---------------------------------------------------------------------------
+// row pass for n = 1024, uint16 frames: gather + real-to-complex FFT.
+// CTA = one scan row r_y x 16 bright-field pixels; the grid runs pixel groups
+// fastest, so neighbouring groups of a scan row read the same frame lines
+// while they are in L2.
+//  gather: the 16 pixels of the row's 1024 frames into a uint16 stage
+//          [pixel][word m] (word m holds samples 2m, 2m+1), the word index
+//          XOR-swizzled by the pixel so that the gather's stores (16 pixels x
+//          2 words per warp) and the FFT's loads (2 pixel rows p, p + 8 per
+//          warp) both fall on 32 distinct banks;
+//  FFT:    16 threads per pixel; the 512-point complex FFT of the halved
+//          packed pairs z[m] = (x[2m] + i x[2m+1]) / 2 as 32 x 16: thread t
+//          takes z[t + 16 n] (n < 32), DFT32 over n -> A[t][k2], times
+//          W512^(t k2), through a padded buffer; thread t then takes
+//          k2 in {t, t + 16}: DFT16 over t' -> Z[k2 + 32 k1];
+//  split:  X[k] = a - i W1024^k b with a = Z[k] + conj Z[512 - k],
+//          b = Z[k] - conj Z[512 - k] (the halving supplies the 1/2),
+//          X[512] = 2 (Re Z[0] - Im Z[0]); written straight to G[k][r_y][q_x].
+// ---------------------------------------------------------------------------
+constexpr int kR1024Pix = 16;
+constexpr int kR1024Threads = 16 * kR1024Pix;
+constexpr int kR1024Words = 512;  // stage words per pixel
+constexpr int kR1024TS = 33;      // transpose stride per t (float2)
+constexpr int kR1024ZS = 16 * kR1024TS;
+constexpr size_t kR1024Smem =
+    (size_t)kR1024Pix * kR1024Words * sizeof(uint32_t) + (size_t)kR1024Pix * kR1024ZS * sizeof(float2);
+
+__device__ __forceinline__ int r1024_word(int p, int m) {
+    return p * kR1024Words + (m ^ ((p & 7) | (((p >> 3) & 1) << 4)));
+}
+
+__global__ void __launch_bounds__(kR1024Threads, 2)
+ssb_row1024(const uint16_t* __restrict__ frames, int det_pix, const int32_t* __restrict__ bf_idx, int n_bf,
+            float2* __restrict__ G, const float2* __restrict__ tw) {
+    constexpr int N = 1024, H = N / 2 + 1;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    uint32_t* stage = reinterpret_cast<uint32_t*>(smem_raw);
+    float2* zb = reinterpret_cast<float2*>(smem_raw + (size_t)kR1024Pix * kR1024Words * sizeof(uint32_t));
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int k0 = blockIdx.x * kR1024Pix;
+    const int ry = blockIdx.y;
+    {
+        const int p = lane & 15, mb = lane >> 4;
+        const int pix = k0 + p < n_bf ? bf_idx[k0 + p] : 0;
+        const uint16_t* src = frames + (size_t)ry * N * det_pix + pix;
+#pragma unroll 8
+        for (int j = 0; j < 32; ++j) {
+            const int m = warp + 8 * mb + 16 * j;
+            const uint32_t lo = __ldcs(src + (size_t)(2 * m) * det_pix);
+            const uint32_t hi = __ldcs(src + (size_t)(2 * m + 1) * det_pix);
+            stage[r1024_word(p, m)] = lo | (hi << 16);
+        }
+    }
+    __syncthreads();
+    const int t = lane & 15, p = warp + 8 * (lane >> 4);
+    float2* zp = zb + p * kR1024ZS;
+    {
+        float2 v[32];
+#pragma unroll
+        for (int n = 0; n < 32; ++n) v[n] = half_pair(stage[r1024_word(p, t + 16 * n)]);
+        Dft<32>::run(v);  // v[k2] = A[t][k2]
+#pragma unroll
+        for (int k2 = 0; k2 < 32; ++k2)
+            zp[t * kR1024TS + k2] = k2 == 0 ? v[0] : cmul(v[k2], __ldg(tw + ((2 * t * k2) & (N - 1))));
+    }
+    __syncwarp();  // a pixel's 16 threads are one half of a warp
+    {
+        float2 a[16], b[16];
+#pragma unroll
+        for (int t2 = 0; t2 < 16; ++t2) {
+            a[t2] = zp[t2 * kR1024TS + t];
+            b[t2] = zp[t2 * kR1024TS + t + 16];
+        }
+        Dft<16>::run(a);  // a[k1] = Z[t + 32 k1]
+        Dft<16>::run(b);  // b[k1] = Z[t + 16 + 32 k1]
+        __syncwarp();
+#pragma unroll
+        for (int k1 = 0; k1 < 16; ++k1) {
+            zp[t + 32 * k1] = a[k1];
+            zp[t + 16 + 32 * k1] = b[k1];
+        }
+    }
+    __syncwarp();
+    const int kp = k0 + p;
+    if (kp < n_bf) {
+        float2* out = G + ((size_t)kp * N + ry) * H;
+#pragma unroll 4
+        for (int j = 0; j < 32; ++j) {
+            const int k = t + 16 * j;
+            const float2 z = zp[k], pr = zp[(512 - k) & 511];
+            const float ax = z.x + pr.x, ay = z.y - pr.y;
+            const float bx = z.x - pr.x, by = z.y + pr.y;
+            const float2 w = __ldg(tw + k);
+            out[k] = make_float2(ax + w.x * by + w.y * bx, ay - w.x * bx + w.y * by);
+        }
+        if (t == 0) out[512] = make_float2(2.0f * (zp[0].x - zp[0].y), 0.0f);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 // column pass of one chunk of planes: the 32 x 32 register kernel at n = 1024,
@@ -277,6 +378,32 @@ static cudaError_t build_n(const T* frames, int det_pix, const int32_t* bf_idx, 
     return cudaSuccess;
 }
 
+// n = 1024, uint16 frames: one row pass over every BF pixel (G written once
+// as the row spectra), then the column pass in place, in launches of at most
+// 65535 planes
+static cudaError_t build_1024_u16(const uint16_t* frames, int det_pix, const int32_t* bf_idx, int n_bf, float2* G,
+                                  const float2* tw, cudaStream_t st) {
+    cudaError_t e;
+    if ((e = cudaFuncSetAttribute(ssb_row1024, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kR1024Smem)) !=
+        cudaSuccess)
+        return e;
+    if ((e = cudaFuncSetAttribute(ssb_col1024, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kC1024Smem)) !=
+        cudaSuccess)
+        return e;
+    ssb_row1024<<<dim3((n_bf + kR1024Pix - 1) / kR1024Pix, 1024), kR1024Threads, kR1024Smem, st>>>(
+        frames, det_pix, bf_idx, n_bf, G, tw);
+    count_launch();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    for (int kb = 0; kb < n_bf; kb += 65535) {
+        const int cnt = n_bf - kb < 65535 ? n_bf - kb : 65535;
+        ssb_col1024<<<dim3((1024 / 2 + 1 + kC1024Cols - 1) / kC1024Cols, cnt), kC1024Threads, kC1024Smem, st>>>(
+            G, kb, tw);
+        count_launch();
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
 template <typename T>
 static cudaError_t build_t(const T* frames, int n, int det_pix, const int32_t* bf_idx, int n_bf,
                            float2* G, const float2* tw, cudaStream_t st) {
@@ -288,7 +415,11 @@ static cudaError_t build_t(const T* frames, int n, int det_pix, const int32_t* b
         case 128: return build_n<128, T>(frames, det_pix, bf_idx, n_bf, G, tw, st);
         case 256: return build_n<256, T>(frames, det_pix, bf_idx, n_bf, G, tw, st);
         case 512: return build_n<512, T>(frames, det_pix, bf_idx, n_bf, G, tw, st);
-        case 1024: return build_n<1024, T>(frames, det_pix, bf_idx, n_bf, G, tw, st);
+        case 1024:
+            if constexpr (std::is_same<T, uint16_t>::value)
+                return build_1024_u16(frames, det_pix, bf_idx, n_bf, G, tw, st);
+            else
+                return build_n<1024, T>(frames, det_pix, bf_idx, n_bf, G, tw, st);
         default: return cudaErrorInvalidValue;
     }
 }

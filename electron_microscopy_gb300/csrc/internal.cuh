@@ -133,6 +133,14 @@ template <> struct Dft<16> {
     }
 };
 
+// packed even/odd samples z = (x[2w], x[2w+1]) / 2 from one 32-bit word of
+// two uint16 counts: 2^23 + u is exact in float, (2^23 + u)/2 - 2^22 = u/2
+__device__ __forceinline__ float2 half_pair(uint32_t u) {
+    const float lo = __fmaf_rn(__uint_as_float(0x4B000000u | (u & 0xFFFFu)), 0.5f, -4194304.0f);
+    const float hi = __fmaf_rn(__uint_as_float(0x4B000000u | (u >> 16)), 0.5f, -4194304.0f);
+    return make_float2(lo, hi);
+}
+
 // cos and sin of 2 pi k / 32, k < 16 (the mathematical values, rounded to
 // float): W32^k = kCos32[k] - i kSin32[k]
 __device__ constexpr float kCos32[16] = {1.0f, 0.98078528040323043f, 0.92387953251128674f, 0.83146961230254524f,

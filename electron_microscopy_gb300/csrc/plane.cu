@@ -124,14 +124,6 @@ __device__ __forceinline__ void discard_l2_line(const void* p) {
     asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
 }
 
-// packed even/odd samples z = (x[2w], x[2w+1]) / 2 from one 32-bit word of
-// two uint16 counts: 2^23 + u is exact in float, (2^23 + u)/2 - 2^22 = u/2
-__device__ __forceinline__ float2 half_pair(uint32_t u) {
-    const float lo = __fmaf_rn(__uint_as_float(0x4B000000u | (u & 0xFFFFu)), 0.5f, -4194304.0f);
-    const float hi = __fmaf_rn(__uint_as_float(0x4B000000u | (u >> 16)), 0.5f, -4194304.0f);
-    return make_float2(lo, hi);
-}
-
 // ---------------------------------------------------------------------------
 // one bright-field pixel's 512 x 512 real-to-complex FFT on a C-CTA cluster;
 // persistent: cluster c handles chunk planes c, c + nclusters, ...

@@ -149,12 +149,18 @@ def test_full_scan_size_float32_frames(ssb):
     _check_against_oracle(ssb, frames, g, AB)
 
 
-def test_max_scan_size_1024(ssb):
+@pytest.mark.parametrize("dtype", [np.uint16, np.float32])
+def test_max_scan_size_1024(ssb, dtype):
+    """n = 1024: the 32 x 32 column kernel for both frame types and, for uint16
+    frames, the 16-pixel row kernel; 31 BF pixels = one full pixel group plus
+    a ragged one."""
     rng = np.random.default_rng(10)
     n, det = 1024, 6
-    frames = rng.poisson(3.0, size=(n, n, det, det)).astype(np.uint16)
-    g = _geom(n, det, 0.6)
-    _check_against_oracle(ssb, frames, g, AB.replace(tilt_x_rad=0.0, tilt_y_rad=0.0))
+    frames = rng.poisson(3.0, size=(n, n, det, det)).astype(dtype)
+    g = _geom(n, det, 0.45)
+    ab = AB.replace(tilt_x_rad=0.0, tilt_y_rad=0.0)
+    assert 16 < len(O.bf_indices(g)) < 32
+    _check_against_oracle(ssb, frames, g, ab)
 
 
 def test_zero_frames_give_zero_G_and_flat_phase(ssb):
