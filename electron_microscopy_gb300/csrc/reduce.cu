@@ -79,7 +79,11 @@ cudaError_t launch_prep(const int32_t* bf_idx, int n_bf, int det_x, double cy, d
 // fused reduction
 // ---------------------------------------------------------------------------
 constexpr int kRedThreads = 256;
-constexpr int kRedUnroll = 4;  // k steps whose loads are issued together
+constexpr int kKChunk = 64;  // k pixels whose tables a block stages at a time
+// k steps whose G loads are issued together: the single-set pass streams G
+// and is bound by load latency, so it keeps more loads in flight
+template <int MAXB>
+__host__ __device__ constexpr int red_unroll() { return MAXB == 1 ? 8 : 4; }
 
 // w(q,k) G(q,k) added to acc: d = chi(k) - chi(k -/+ q) in turns, reduced to
 // [-1/2, 1/2] exactly.  T-: w = exp(-2 pi i d); T+: w = -exp(+2 pi i d), which
@@ -194,7 +198,7 @@ ssb_reduce(RedLaunch P, SetBatch sb) {
         }
     };
 
-    auto step = [&](float2 g, float4 kd, int k, auto tab) {
+    auto step = [&](float2 g, float4 kd, const float* chk, auto tab) {
         if (decltype(tab)::value && kd.y != cur_ky) {  // uniform: every lane walks the same k
             new_row(kd.y);
             cur_ky = kd.y;
@@ -232,10 +236,10 @@ ssb_reduce(RedLaunch P, SetBatch sb) {
                     const float tw = m ? kTwoPi : -kTwoPi;
                     cnt[0] += 1;
                     float ck[MAXB];
-                    const float4* cp = reinterpret_cast<const float4*>(P.chik + (size_t)k * kChiStride);
+                    const float4* cp = reinterpret_cast<const float4*>(chk);
 #pragma unroll
                     for (int v4 = 0; v4 < (MAXB + 3) / 4; ++v4) {
-                        const float4 c4 = __ldg(cp + v4);
+                        const float4 c4 = cp[v4];
                         ck[4 * v4] = c4.x;
                         if (4 * v4 + 1 < MAXB) ck[4 * v4 + 1] = c4.y;
                         if (4 * v4 + 2 < MAXB) ck[4 * v4 + 2] = c4.z;
@@ -255,7 +259,7 @@ ssb_reduce(RedLaunch P, SetBatch sb) {
                     const bool p = aperture_f32(px, py, sb.s[s].tx, sb.s[s].ty, sb.r2, &pvx, &pvy);
                     if (m != p) {
                         const float cq = chi_v(tab, s, m, m ? mvx : pvx, m ? mvy : pvy);
-                        accumulate(acc[s], side_sign(g, m), __ldg(P.chik + (size_t)k * kChiStride + s), cq,
+                        accumulate(acc[s], side_sign(g, m), chk[s], cq,
                                    m ? kTwoPi : -kTwoPi);
                         cnt[s] += 1;
                     }
@@ -264,30 +268,45 @@ ssb_reduce(RedLaunch P, SetBatch sb) {
         }
     };
 
-    auto walk = [&](auto tab) {
-        int k = kb;
+    // the k tables of a chunk of kKChunk pixels are staged in shared memory by
+    // the whole block (every thread walks the same k), so a step reads them
+    // as short broadcasts and the registers go to G loads in flight
+    __shared__ float4 s_ktab[kKChunk];
+    __shared__ float4 s_chik[MAXB > 1 ? kKChunk * kChiStride / 4 : 1];
+    auto walk = [&](auto tab, int kc0, int kcn) {
+        constexpr int U = red_unroll<MAXB>();
+        const float2* gk = gp + (size_t)kc0 * plane;
+        int i = 0;
 #pragma unroll 1
-        for (; k + kRedUnroll <= ke; k += kRedUnroll) {
-            float2 g[kRedUnroll];
-            float4 kd[kRedUnroll];
+        for (; i + U <= kcn; i += U) {
+            float2 g[U];
 #pragma unroll
-            for (int u = 0; u < kRedUnroll; ++u) {
-                g[u] = valid ? __ldcs(gp + (size_t)(k + u) * plane) : make_float2(0.f, 0.f);
-                kd[u] = __ldg(P.ktab + k + u);
-            }
+            for (int u = 0; u < U; ++u) g[u] = valid ? __ldcs(gk + (size_t)(i + u) * plane) : make_float2(0.f, 0.f);
 #pragma unroll
-            for (int u = 0; u < kRedUnroll; ++u) step(g[u], kd[u], k + u, tab);
+            for (int u = 0; u < U; ++u)
+                step(g[u], s_ktab[i + u], reinterpret_cast<const float*>(s_chik) + (i + u) * kChiStride, tab);
         }
 #pragma unroll 1
-        for (; k < ke; ++k) {
-            const float2 g = valid ? __ldcs(gp + (size_t)k * plane) : make_float2(0.f, 0.f);
-            step(g, __ldg(P.ktab + k), k, tab);
+        for (; i < kcn; ++i) {
+            const float2 g = valid ? __ldcs(gk + (size_t)i * plane) : make_float2(0.f, 0.f);
+            step(g, s_ktab[i], reinterpret_cast<const float*>(s_chik) + i * kChiStride, tab);
         }
     };
-    if (MAXB == 1 || row_table)
-        walk(std::true_type{});
-    else
-        walk(std::false_type{});
+#pragma unroll 1
+    for (int kc0 = kb; kc0 < ke; kc0 += kKChunk) {
+        const int kcn = min(kKChunk, ke - kc0);
+        __syncthreads();  // every read of the previous chunk's tables is done
+        for (int i = threadIdx.x; i < kcn; i += kRedThreads) s_ktab[i] = __ldg(P.ktab + kc0 + i);
+        if constexpr (MAXB > 1) {
+            const float4* src = reinterpret_cast<const float4*>(P.chik) + (size_t)kc0 * (kChiStride / 4);
+            for (int i = threadIdx.x; i < kcn * (kChiStride / 4); i += kRedThreads) s_chik[i] = __ldg(src + i);
+        }
+        __syncthreads();
+        if (MAXB == 1 || row_table)
+            walk(std::true_type{}, kc0, kcn);
+        else
+            walk(std::false_type{}, kc0, kcn);
+    }
     if (valid) {
 #pragma unroll
         for (int s = 0; s < MAXB; ++s) {
