@@ -295,7 +295,7 @@ int ssb_build_G(const void* frames, int dtype, const ssb_geometry* geom, const i
     float2* tw = at<float2>(ws, Lw.tw);
     cudaError_t e;
     if ((e = launch_twiddles(tw, geom->n, st)) != cudaSuccess) return cuda_fail(e, "twiddles");
-    if (geom->n == 512 && dtype == SSB_U16 && plane512_clusters() > 0)
+    if (geom->n == 512 && dtype == SSB_U16 && plane512_cluster_size() > 0)
         e = launch_build512(static_cast<const uint16_t*>(frames), geom->det_y * geom->det_x, bf_idx_dev, n_bf,
                             static_cast<float2*>(G_dev), tw, at<void>(ws, Lw.xbuf), st);
     else

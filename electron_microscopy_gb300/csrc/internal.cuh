@@ -338,10 +338,10 @@ cudaError_t launch_build(const void* frames, int dtype, int n, int det_pix,
 cudaError_t launch_crop_idx(const int32_t* in, int n, int det_x, int r0, int c0, int cols, int32_t* out,
                             cudaStream_t st);
 // n = 512, uint16 frames: gather + cluster FFT (plane.cu); xbuf holds
-// plane512_chunk_bytes(); plane512_clusters() is 0 when the cluster kernel
+// plane512_chunk_bytes(); plane512_cluster_size() is 0 when the cluster kernel
 // cannot be scheduled on the current device
 size_t plane512_chunk_bytes();
-int plane512_clusters();
+int plane512_cluster_size();
 cudaError_t launch_build512(const uint16_t* frames, int det_pix, const int32_t* bf_idx, int n_bf,
                             float2* G, const float2* tw, void* xbuf, cudaStream_t st);
 

@@ -455,7 +455,7 @@ static int plane_clusters() {
 // planes of the 512^2 x 9354 workload), so the portable form is kept.
 static int plane_cluster_size() { return plane_clusters<8>() > 0 ? 8 : 0; }
 
-int plane512_clusters() { return plane_cluster_size(); }
+int plane512_cluster_size() { return plane_cluster_size(); }
 
 // two gather buffers of 64 planes, two exchange slots per cluster
 size_t plane512_chunk_bytes() {
