@@ -222,7 +222,7 @@ def build_G_host_bytes(geom, bf_idx_host, dtype) -> int:
 
 def build_G_host(frames_host, geom, bf_idx_host, bf_idx_dev, G=None, ws=None, stream=None):
     """G(q,k) from frames in host memory (a CPU tensor, pinned for full copy
-    speed): only the detector rows holding bright-field pixels are copied.
+    speed): only the bounding box of the bright-field pixels on the detector is copied.
     bf_idx_host (numpy int32) and bf_idx_dev hold the same indices.  The copy
     is asynchronous on `stream`: keep frames_host alive and unchanged until
     the stream has passed it."""
