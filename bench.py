@@ -468,6 +468,32 @@ def run_ours(args, ws, rank, local, pg):
     clk_mhz = (clk or {}).get("sm_mhz") or 2070.0
     xu_peak = 16.0 * sms * clk_mhz * 1e6
     xu_ach = 2.0 * terms / (score_ms * 1e-3)
+    # the batched-scoring configuration: B = 1, 2, 4, 8 sets per pass (after
+    # the timed region; 10 passes each, CUDA events on the launching stream)
+    score_sweep = {}
+    for Bs in (1, 2, 4, 8):
+        sub = sets[:Bs]
+        Ob_s = torch.empty((Bs, nq), dtype=torch.complex64, device=dev)
+        Nb_s = torch.empty((Bs, nq), dtype=torch.int32, device=dev)
+        sc_s = torch.empty((Bs,), dtype=torch.float64, device=dev)
+        ws_b2 = ssb.Workspace(ssb.workspace_bytes(geom, n_bf, ssb.OP_SCORE, Bs, nq), dev)
+        run = lambda: ssb.score_batch(G, geom, bfd, sub, band_d, O=Ob_s, N=Nb_s, score=sc_s, ws=ws_b2,  # noqa: E731
+                                      stream=stream)
+        for _ in range(3):
+            run()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(10):
+            run()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t_ms = e0.elapsed_time(e1) / 10
+        terms_b = int(Nb_s.sum().item())
+        score_sweep[str(Bs)] = {"ms": t_ms, "terms": terms_b, "terms_per_s": terms_b / (t_ms * 1e-3),
+                                "xu_frac": 2.0 * terms_b / (t_ms * 1e-3) / xu_peak,
+                                "hbm_frac": bytes_score / (t_ms * 1e-3) / 1e9 / hbm}
+        del ws_b2
+
     stage_rooflines = {
         "reconstruct": {"bound": "hbm", "achieved": bytes_recon / (recon_ms * 1e-3) / 1e9, "peak": hbm,
                         "unit": "GB/s", "frac": bytes_recon / (recon_ms * 1e-3) / 1e9 / hbm,
@@ -496,6 +522,7 @@ def run_ours(args, ws, rank, local, pg):
                    "score_terms": terms, "score_terms_per_s": terms / (score_ms * 1e-3),
                    "max_count": d.get("max_count")},
         "stage_rooflines": stage_rooflines,
+        "score_sweep": score_sweep,
         "roofline": {"bound": "hbm", "kernel": "ssb_build_G = ssb_gather + ssb_plane512<8> on two internal streams (one C-ABI call, timed on the caller's stream)", "achieved": achieved,
                      "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
                      "peak_source": peak_src, "algorithmic_bytes": bytes_build},
