@@ -262,12 +262,19 @@ ssb_row1024(const uint16_t* __restrict__ frames, int det_pix, const int32_t* __r
         const int p = lane & 15, mb = lane >> 4;
         const int pix = k0 + p < n_bf ? bf_idx[k0 + p] : 0;
         const uint16_t* src = frames + (size_t)ry * N * det_pix + pix;
-#pragma unroll 8
+        // all of a thread's 64 loads in flight (registers are idle here)
+        uint32_t wv[32];
+#pragma unroll
         for (int j = 0; j < 32; ++j) {
             const int m = warp + 8 * mb + 16 * j;
             const uint32_t lo = __ldcs(src + (size_t)(2 * m) * det_pix);
             const uint32_t hi = __ldcs(src + (size_t)(2 * m + 1) * det_pix);
-            stage[r1024_word(p, m)] = lo | (hi << 16);
+            wv[j] = lo | (hi << 16);
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int m = warp + 8 * mb + 16 * j;
+            stage[r1024_word(p, m)] = wv[j];
         }
     }
     __syncthreads();
