@@ -35,7 +35,7 @@ METRIC = "ms per SSB recon + G-build HBM GB/s (512^2 scan, 192^2 det, ~9.3k BF p
 # DRAM bytes (read + write) of one ssb_build_G call on the full workload, from
 # the ncu capture summarised in profiles/build_traffic_full.md, valid for the
 # build kernels' source with this SHA-256 prefix only (null otherwise)
-BUILD_TRAFFIC = {"plane_cu_sha256": "4c21b83e86d06bf4", "bytes": 26.47e9}
+BUILD_TRAFFIC = {"plane_cu_sha256": "4c9af9fd23038508", "bytes": 26.47e9}
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -50,6 +50,7 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=8)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-sweep", action="store_true", help="skip the B = 1, 2, 4, 8 scoring sweep")
     p.add_argument("--cpu-sample-bf", type=int, default=0, help="BF pixels in the oracle sample (0: auto)")
     return p.parse_args()
 
@@ -471,7 +472,7 @@ def run_ours(args, ws, rank, local, pg):
     # the batched-scoring configuration: B = 1, 2, 4, 8 sets per pass (after
     # the timed region; 10 passes each, CUDA events on the launching stream)
     score_sweep = {}
-    for Bs in (1, 2, 4, 8):
+    for Bs in (() if args.no_sweep else (1, 2, 4, 8)):
         sub = sets[:Bs]
         Ob_s = torch.empty((Bs, nq), dtype=torch.complex64, device=dev)
         Nb_s = torch.empty((Bs, nq), dtype=torch.int32, device=dev)
