@@ -5,19 +5,21 @@
 // "Historical WebGPU G(q,k) memory experiment", sections "Why herm is exactly
 // lossless" and "Implementation").
 //
-// Two passes per chunk of bright-field pixels:
-//   row pass    one CTA per (scan row r_y, 32 BF pixels): gathers the 32
-//               pixels from the n frames of that scan row (each warp load
-//               reads 32 neighbouring detector pixels of one frame), transposes
-//               them through shared memory, runs the real-to-complex FFT along
-//               r_x (n/2-point complex FFT of the packed even/odd samples plus
-//               the split step) and writes the n/2+1 outputs into G's row r_y;
-//   column pass one CTA per (BF pixel, group of 16 q_x columns): loads the
-//               columns, runs the complex FFT along r_y and writes them back in
-//               place.
-// The host walks the BF pixels in chunks and issues row(c) and column(c-1)
-// back to back so that a chunk's intermediate rows are still in L2 when the
-// column pass reads them.
+// Every size except n = 512 with uint16 frames (plane.cu) builds G in two
+// passes over it: a row pass (gather + real-to-complex FFT along r_x of the
+// packed even/odd samples, plus the split step, written as G's rows) and a
+// column pass (complex FFT along r_y, in place).
+//  - general n: row pass one CTA per (scan row r_y, 32 BF pixels), gathering
+//    the 32 pixels from the n frames of that scan row, transposing them through
+//    shared memory and running a warp-level Stockham FFT; column pass one CTA
+//    per (BF pixel, 16 q_x columns), Stockham in shared memory.  The host walks
+//    the BF pixels in chunks and issues row(c) and column(c-1) back to back so
+//    that a chunk's rows are still in L2 when the column pass reads them.
+//  - n = 1024: the column pass is ssb_col1024 (32 x 32 in registers, 8 columns
+//    per CTA); with uint16 frames the row pass is ssb_row1024 (16 pixels per
+//    CTA, 32 x 16 in registers), one launch over all BF pixels.
+// The host-input build (ssb_build_G_host) first remaps the indices into the
+// copied detector box (ssb_crop_idx).
 #include <type_traits>
 
 #include "internal.cuh"
