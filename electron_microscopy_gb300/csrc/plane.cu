@@ -42,7 +42,7 @@
 namespace ssb {
 
 constexpr int kGatherThreads = 256;
-constexpr int kGatherFrames = 128;  // scan positions per gather CTA
+constexpr int kGatherFrames = 64;  // scan positions per gather CTA
 
 template <typename T>
 __host__ __device__ constexpr int gather_pixels() { return sizeof(T) == 2 ? 64 : 32; }
