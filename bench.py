@@ -35,7 +35,7 @@ METRIC = "ms per SSB recon + G-build HBM GB/s (512^2 scan, 192^2 det, ~9.3k BF p
 # DRAM bytes (read + write) of one ssb_build_G call on the full workload, from
 # the ncu capture summarised in profiles/build_traffic_full.md, valid for the
 # build kernels' source with this SHA-256 prefix only (null otherwise)
-BUILD_TRAFFIC = {"plane_cu_sha256": "4c9af9fd23038508", "bytes": 26.47e9}
+BUILD_TRAFFIC = {"plane_cu_sha256": "b845ca1145fa8310", "bytes": 26.80e9}
 L2_BYTES = 129 * 1024 * 1024
 
 
