@@ -361,3 +361,95 @@ def score_sets(G, geom, sets, bf_idx, band):
         O, N = reduce(G, geom, ab, bf_idx, entries=band)
         out.append((O, N, score(O, N)))
     return out
+
+
+# ----------------------------------------------------------------------------
+# compact G storage: herm16 (snorm16 codes + float32 block scales) and the
+# band-compacted copy
+# ----------------------------------------------------------------------------
+# Sources: "Historical WebGPU G(q,k) memory experiment", section
+# "Implementation": a post-pass over the built half plane first takes the
+# per-BF-pixel maximum of |G| (scaleMax), then stores each component as
+# pack2x16snorm(clamp(v / scale)); a reader multiplies unpack2x16snorm(word) by
+# the pixel's scale.  Section "Memory planning table": active_BF * N * (N/2+1)
+# * 4 bytes plus 4 bytes per BF pixel.  Section "Scan-size sweep", conclusions,
+# and "Lessons learned" item 3: per-q-row block scales (n scales per BF pixel)
+# as the follow-up that bounds the dynamic range inside each block.
+#
+# READING pack2x16snorm (the WGSL built-in the page names): component e is
+# stored as the 16-bit two's complement integer floor(0.5 + 32767 * clamp(e,
+# -1, 1)), component 0 (real) in bits 0-15 and component 1 (imaginary) in bits
+# 16-31; unpack2x16snorm gives max(c / 32767, -1).
+# READING precision: the pages fix none; scale, quotient and code are taken in
+# float32 (the kernel's precision), each operation rounded once, so the integer
+# codes are decided in the same precision on both sides.
+# READING |G|: the complex modulus, sqrt(re^2 + im^2).  max |G| = sqrt(max
+# re^2 + im^2) since a correctly rounded sqrt is monotone.
+# READING empty block: a block whose max |G| is 0 stores scale 0 and codes 0.
+# READING block shapes: rows_per_scale = n (one scale per BF pixel, the page's
+# preview) or 1 (one scale per q row of the half plane, the follow-up).
+# Scales are laid out [n / rows_per_scale][N_bf].
+
+SNORM16_MAX = 32767
+
+
+def herm16_scales(G32, rows_per_scale):
+    """max |G| per (row block, BF pixel) in float32: array (n/rows, N_bf)."""
+    G32 = np.asarray(G32, dtype=np.complex64)
+    nbf, n, h = G32.shape
+    if rows_per_scale not in (1, n):
+        raise ValueError("rows_per_scale must be 1 or n")
+    x = G32.real.astype(np.float32)
+    y = G32.imag.astype(np.float32)
+    m2 = x * x + y * y                                   # float32, one rounding per op
+    blocks = n // rows_per_scale
+    m2 = m2.reshape(nbf, blocks, rows_per_scale * h).max(axis=2)
+    return np.sqrt(m2).T.copy()                          # (blocks, N_bf) float32
+
+
+def _snorm16(v, s):
+    """floor(0.5 + 32767 clamp(v / s, -1, 1)) in float32; 0 where s == 0."""
+    v = np.asarray(v, dtype=np.float32)
+    s = np.asarray(s, dtype=np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        e = np.where(s > 0, v / np.where(s > 0, s, np.float32(1)), np.float32(0)).astype(np.float32)
+    e = np.minimum(np.float32(1), np.maximum(np.float32(-1), e))
+    c = np.floor(np.float32(0.5) + np.float32(SNORM16_MAX) * e)
+    return c.astype(np.int16)
+
+
+def herm16_pack(G32, rows_per_scale):
+    """(codes int16 (N_bf, n, n/2+1, 2) [re, im], scales float32 (n/rows, N_bf))."""
+    G32 = np.asarray(G32, dtype=np.complex64)
+    nbf, n, h = G32.shape
+    sc = herm16_scales(G32, rows_per_scale)
+    # scale of entry (k, row, col): block row // rows_per_scale
+    s_full = np.repeat(sc.T, rows_per_scale, axis=1)[:, :, None]      # (N_bf, n, 1)
+    codes = np.empty((nbf, n, h, 2), dtype=np.int16)
+    codes[..., 0] = _snorm16(G32.real, s_full)
+    codes[..., 1] = _snorm16(G32.imag, s_full)
+    return codes, sc
+
+
+def herm16_unpack(codes, scales, rows_per_scale):
+    """complex128 G~ = max(c / 32767, -1) * scale, per component."""
+    codes = np.asarray(codes)
+    nbf, n, h, _ = codes.shape
+    s_full = np.repeat(np.asarray(scales, dtype=np.float64).T, rows_per_scale, axis=1)[:, :, None]
+    u = np.maximum(codes.astype(np.float64) / SNORM16_MAX, -1.0)
+    return (u[..., 0] + 1j * u[..., 1]) * s_full
+
+
+def herm16_bytes(nbf, n, rows_per_scale):
+    """Stored bytes: 4 per half-plane entry plus 4 per scale."""
+    return nbf * n * (n // 2 + 1) * 4 + (n // rows_per_scale) * nbf * 4
+
+
+def band_compact(G, band):
+    """The band entries of every BF pixel's half plane, in band order:
+    (N_bf, n, n/2+1, ...) -> (N_bf, nq, ...).  No page describes this copy;
+    the scoring passes of a fit ("Tilt-corrected SSB on CUDA", section "Where
+    the time went": 78 passes) read only these entries."""
+    G = np.asarray(G)
+    nbf, n, h = G.shape[:3]
+    return G.reshape((nbf, n * h) + G.shape[3:])[:, np.asarray(band, dtype=np.int64)]
