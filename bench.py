@@ -51,6 +51,8 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-sweep", action="store_true", help="skip the B = 1, 2, 4, 8 scoring sweep")
+    p.add_argument("--no-compact", action="store_true",
+                   help="skip the compact-storage measurements (band copy, herm16)")
     p.add_argument("--cpu-sample-bf", type=int, default=0, help="BF pixels in the oracle sample (0: auto)")
     return p.parse_args()
 
@@ -469,31 +471,86 @@ def run_ours(args, ws, rank, local, pg):
     clk_mhz = (clk or {}).get("sm_mhz") or 2070.0
     xu_peak = 16.0 * sms * clk_mhz * 1e6
     xu_ach = 2.0 * terms / (score_ms * 1e-3)
-    # the batched-scoring configuration: B = 1, 2, 4, 8 sets per pass (after
-    # the timed region; 10 passes each, CUDA events on the launching stream)
-    score_sweep = {}
-    for Bs in (() if args.no_sweep else (1, 2, 4, 8)):
-        sub = sets[:Bs]
-        Ob_s = torch.empty((Bs, nq), dtype=torch.complex64, device=dev)
-        Nb_s = torch.empty((Bs, nq), dtype=torch.int32, device=dev)
-        sc_s = torch.empty((Bs,), dtype=torch.float64, device=dev)
-        ws_b2 = ssb.Workspace(ssb.workspace_bytes(geom, n_bf, ssb.OP_SCORE, Bs, nq), dev)
-        run = lambda: ssb.score_batch(G, geom, bfd, sub, band_d, O=Ob_s, N=Nb_s, score=sc_s, ws=ws_b2,  # noqa: E731
-                                      stream=stream)
-        for _ in range(3):
+    def timed(run, reps=10, warm=3):
+        """mean ms of `run` over `reps` calls, CUDA events on the launching stream"""
+        for _ in range(warm):
             run()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(10):
+        for _ in range(reps):
             run()
         e1.record(stream)
         torch.cuda.synchronize()
-        t_ms = e0.elapsed_time(e1) / 10
-        terms_b = int(Nb_s.sum().item())
-        score_sweep[str(Bs)] = {"ms": t_ms, "terms": terms_b, "terms_per_s": terms_b / (t_ms * 1e-3),
-                                "xu_frac": 2.0 * terms_b / (t_ms * 1e-3) / xu_peak,
-                                "hbm_frac": bytes_score / (t_ms * 1e-3) / 1e9 / hbm}
-        del ws_b2
+        return e0.elapsed_time(e1) / reps
+
+    def sweep(store, band_bytes):
+        """B = 1, 2, 4, 8 sets per scoring pass over the band (10 passes each);
+        store None: the complex64 half plane through ssb_score_batch"""
+        out = {}
+        for Bs in (1, 2, 4, 8):
+            sub = sets[:Bs]
+            Ob_s = torch.empty((Bs, nq), dtype=torch.complex64, device=dev)
+            Nb_s = torch.empty((Bs, nq), dtype=torch.int32, device=dev)
+            sc_s = torch.empty((Bs,), dtype=torch.float64, device=dev)
+            ws_b2 = ssb.Workspace(ssb.workspace_bytes(geom, n_bf, ssb.OP_SCORE, Bs, nq), dev)
+            if store is None:
+                run = lambda: ssb.score_batch(G, geom, bfd, sub, band_d, O=Ob_s, N=Nb_s, score=sc_s,  # noqa: E731
+                                              ws=ws_b2, stream=stream)
+            else:
+                run = lambda: ssb.score_batch_g(store, geom, bfd, sub, band_d, O=Ob_s, N=Nb_s,  # noqa: E731
+                                                score=sc_s, ws=ws_b2, stream=stream)
+            t_ms = timed(run)
+            terms_b = int(Nb_s.sum().item())
+            out[str(Bs)] = {"ms": t_ms, "terms": terms_b, "terms_per_s": terms_b / (t_ms * 1e-3),
+                            "xu_frac": 2.0 * terms_b / (t_ms * 1e-3) / xu_peak,
+                            "hbm_frac": band_bytes / (t_ms * 1e-3) / 1e9 / hbm}
+            del ws_b2
+        return out
+
+    # the batched-scoring configuration: B = 1, 2, 4, 8 sets per pass (after
+    # the timed region)
+    score_sweep = {} if args.no_sweep else sweep(None, bytes_score)
+
+    # compact G storage (measured after the timed region, not part of the
+    # step): the band-compacted complex64 copy, and herm16 with one scale per
+    # q row or per BF pixel -- the packing pass, the reconstruction from it and
+    # the scoring sweep over its band copy.  Algorithmic bytes: what each pass
+    # must read and write once.
+    compact = None
+    if not args.no_compact:
+        compact = {}
+        entries = n_bf * n * h
+        Gb = torch.empty((n_bf, nq), dtype=torch.complex64, device=dev)
+        src = ssb.GStore(G)
+        t_band = timed(lambda: ssb.compact_band(src, geom, band_d, dst=Gb, stream=stream), reps=5)
+        bb = n_bf * nq * 8
+        compact["band_c64"] = {
+            "copy_ms": t_band, "copy_GBs": 2 * bb / (t_band * 1e-3) / 1e9,
+            "copy_hbm_frac": 2 * bb / (t_band * 1e-3) / 1e9 / hbm, "copy_algorithmic_bytes": 2 * bb,
+            "score_sweep": sweep(ssb.GStore(Gb, band_compact=True), bb)}
+        del Gb
+        Oc, Nc, phc = torch.empty_like(Od), torch.empty_like(Nd), torch.empty_like(ph)
+        for rows, name in ((1, "herm16_q_row"), (n, "herm16_bf")):
+            W = torch.empty((n_bf, n, h), dtype=torch.int32, device=dev)
+            S = torch.empty((n // rows, n_bf), dtype=torch.float32, device=dev)
+            t_pack = timed(lambda: ssb.compact_G16(G, geom, rows, G16=W, scale=S, stream=stream), reps=5)
+            st = ssb.GStore(W, ssb.G_SN16, S, rows)
+            pack_bytes = entries * 8 + entries * 4 + S.numel() * 4
+            t_rec = timed(lambda: ssb.reconstruct_g(st, geom, bfd, ab, O=Oc, N=Nc, phase=phc, ws=ws_r,
+                                                    stream=stream))
+            rec_bytes = entries * 4 + S.numel() * 4
+            Wb = torch.empty((n_bf, nq), dtype=torch.int32, device=dev)
+            ssb.compact_band(st, geom, band_d, dst=Wb, stream=stream)
+            bb16 = n_bf * nq * 4
+            compact[name] = {
+                "rows_per_scale": rows,
+                "pack_ms": t_pack, "pack_GBs": pack_bytes / (t_pack * 1e-3) / 1e9,
+                "pack_hbm_frac": pack_bytes / (t_pack * 1e-3) / 1e9 / hbm, "pack_algorithmic_bytes": pack_bytes,
+                "recon_ms": t_rec, "recon_GBs": rec_bytes / (t_rec * 1e-3) / 1e9,
+                "recon_hbm_frac": rec_bytes / (t_rec * 1e-3) / 1e9 / hbm, "recon_algorithmic_bytes": rec_bytes,
+                "band_score_sweep": sweep(ssb.GStore(Wb, ssb.G_SN16, S, rows, band_compact=True), bb16)}
+            del W, S, Wb, st
+        torch.cuda.synchronize()
 
     stage_rooflines = {
         "reconstruct": {"bound": "hbm", "achieved": bytes_recon / (recon_ms * 1e-3) / 1e9, "peak": hbm,
@@ -524,6 +581,7 @@ def run_ours(args, ws, rank, local, pg):
                    "max_count": d.get("max_count")},
         "stage_rooflines": stage_rooflines,
         "score_sweep": score_sweep,
+        "compact": compact,
         "roofline": {"bound": "hbm", "kernel": "ssb_build_G = ssb_gather + ssb_plane512<8> on two internal streams (one C-ABI call, timed on the caller's stream)", "achieved": achieved,
                      "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
                      "peak_source": peak_src, "algorithmic_bytes": bytes_build},

@@ -34,7 +34,10 @@ STATUS_NAMES = {0: "SSB_OK", 1: "SSB_INVALID_ARG", 2: "SSB_UNSUPPORTED",
 
 EXPORTED = ("ssb_bf_indices", "ssb_band_indices", "ssb_workspace_bytes", "ssb_build_G",
             "ssb_reconstruct", "ssb_score_batch", "ssb_last_error", "ssb_launch_count",
-            "ssb_reconstruct_noalloc", "ssb_build_G_host", "ssb_build_G_host_bytes")
+            "ssb_reconstruct_noalloc", "ssb_build_G_host", "ssb_build_G_host_bytes",
+            "ssb_compact_G16", "ssb_compact_band", "ssb_reconstruct_g", "ssb_score_batch_g")
+
+G_C64, G_SN16 = 0, 1
 
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
@@ -52,6 +55,28 @@ ABERR_FIELDS = ("C10", "C12a", "C12b", "C21a", "C21b", "C23a", "C23b", "C30", "C
 
 class Aberr(ctypes.Structure):
     _fields_ = [(f, ctypes.c_double) for f in ABERR_FIELDS]
+
+
+class GStoreC(ctypes.Structure):
+    """ssb_gstore: a stored G as the reductions read it."""
+    _fields_ = [("G", ctypes.c_void_p), ("fmt", ctypes.c_int), ("scale", ctypes.c_void_p),
+                ("rows_per_scale", ctypes.c_int), ("band_compact", ctypes.c_int)]
+
+
+class GStore:
+    """Device tensors of a stored G: complex64 [n_bf, n, n/2+1] (fmt G_C64) or
+    herm16 words int32 [n_bf, n, n/2+1] with float32 scales
+    [n / rows_per_scale, n_bf] (fmt G_SN16); band_compact: the last two axes
+    are one band axis [n_bf, nq] (made by compact_band)."""
+
+    def __init__(self, G, fmt=G_C64, scale=None, rows_per_scale=0, band_compact=False):
+        self.G, self.fmt, self.scale = G, fmt, scale
+        self.rows_per_scale, self.band_compact = rows_per_scale, bool(band_compact)
+
+    def c(self) -> GStoreC:
+        return GStoreC(int(self.G.data_ptr()), self.fmt,
+                       int(self.scale.data_ptr()) if self.scale is not None else 0,
+                       self.rows_per_scale, 1 if self.band_compact else 0)
 
 
 class SSBError(RuntimeError):
@@ -88,10 +113,17 @@ def load(path: str | None = None):
     lib.ssb_score_batch.argtypes = [c_vp, G_p, c_vp, c_int, A_p, c_int, c_vp, c_int, c_vp, c_vp, c_vp,
                                     c_vp, c_size, c_vp]
     lib.ssb_reconstruct_noalloc.argtypes = [c_vp, G_p, c_vp, c_int, A_p, c_vp, c_vp, c_vp, c_vp]
+    S_p = ctypes.POINTER(GStoreC)
+    lib.ssb_compact_G16.argtypes = [c_vp, G_p, c_int, c_int, c_vp, c_vp, c_vp]
+    lib.ssb_compact_band.argtypes = [S_p, G_p, c_int, c_vp, c_int, c_vp, c_vp]
+    lib.ssb_reconstruct_g.argtypes = [S_p, G_p, c_vp, c_int, A_p, c_vp, c_vp, c_vp, c_vp, c_size, c_vp]
+    lib.ssb_score_batch_g.argtypes = [S_p, G_p, c_vp, c_int, A_p, c_int, c_vp, c_int, c_vp, c_vp, c_vp,
+                                      c_vp, c_size, c_vp]
     lib.ssb_last_error.restype = ctypes.c_char_p
     lib.ssb_launch_count.restype = ctypes.c_longlong
     for fn in ("ssb_bf_indices", "ssb_band_indices", "ssb_build_G", "ssb_build_G_host", "ssb_reconstruct",
-               "ssb_score_batch", "ssb_reconstruct_noalloc"):
+               "ssb_score_batch", "ssb_reconstruct_noalloc", "ssb_compact_G16", "ssb_compact_band",
+               "ssb_reconstruct_g", "ssb_score_batch_g"):
         getattr(lib, fn).restype = c_int
     _lib = lib
     return lib
@@ -312,3 +344,88 @@ def reconstruct_noalloc(G, geom, bf_idx_dev, aberr, O=None, N=None, phase=None, 
         _ptr(G), ctypes.byref(g), _ptr(bf_idx_dev), n_bf, ctypes.byref(a), _ptr(O), _ptr(N), _ptr(phase),
         _stream(stream)))
     return O, N, phase
+
+
+# ----------------------------------------------------------------------------
+# compact storage of G
+# ----------------------------------------------------------------------------
+
+def compact_G16(G, geom, rows_per_scale, G16=None, scale=None, stream=None) -> GStore:
+    """herm16 of a complex64 G [n_bf, n, n/2+1]: int32 words (real code in the
+    low 16 bits) and float32 scales [n / rows_per_scale, n_bf]; rows_per_scale
+    is n (one scale per BF pixel) or 1 (one per q row)."""
+    import torch
+    lib = load()
+    g = to_geometry(geom)
+    n_bf = int(G.shape[0])
+    dev = G.device
+    G16 = torch.empty(G.shape, dtype=torch.int32, device=dev) if G16 is None else G16
+    nblk = g.n // rows_per_scale if rows_per_scale in (1, g.n) else 1
+    scale = torch.empty((nblk, n_bf), dtype=torch.float32, device=dev) if scale is None else scale
+    _check("ssb_compact_G16", lib.ssb_compact_G16(_ptr(G), ctypes.byref(g), n_bf, rows_per_scale, _ptr(G16),
+                                                  _ptr(scale), _stream(stream)))
+    return GStore(G16, G_SN16, scale, rows_per_scale)
+
+
+def compact_band(src, geom, band_dev, dst=None, stream=None) -> GStore:
+    """Band-compacted copy [n_bf, nq] of a half-plane G (a GStore or a complex64
+    tensor); a herm16 copy keeps the source's scales."""
+    import torch
+    lib = load()
+    if not isinstance(src, GStore):
+        src = GStore(src)
+    g = to_geometry(geom)
+    n_bf = int(src.G.shape[0])
+    nq = int(band_dev.numel())
+    if dst is None:
+        dst = torch.empty((n_bf, nq), dtype=src.G.dtype, device=src.G.device)
+    sc = src.c()
+    _check("ssb_compact_band", lib.ssb_compact_band(ctypes.byref(sc), ctypes.byref(g), n_bf, _ptr(band_dev), nq,
+                                                    _ptr(dst), _stream(stream)))
+    return GStore(dst, src.fmt, src.scale, src.rows_per_scale, band_compact=True)
+
+
+def reconstruct_g(store, geom, bf_idx_dev, aberr, O=None, N=None, phase=None, ws=None, stream=None):
+    """reconstruct() from a GStore (half plane, either format)."""
+    import torch
+    lib = load()
+    g = to_geometry(geom)
+    a = to_aberr(aberr)
+    n_bf = int(bf_idx_dev.numel())
+    n, h = g.n, g.n // 2 + 1
+    dev = store.G.device
+    O = torch.empty((n, h), dtype=torch.complex64, device=dev) if O is None else O
+    N = torch.empty((n, h), dtype=torch.int32, device=dev) if N is None else N
+    phase = torch.empty((n, n), dtype=torch.float32, device=dev) if phase is None else phase
+    if ws is None:
+        ws = Workspace(workspace_bytes(g, n_bf, OP_RECON), dev)
+    sc = store.c()
+    _check("ssb_reconstruct_g", lib.ssb_reconstruct_g(ctypes.byref(sc), ctypes.byref(g), _ptr(bf_idx_dev), n_bf,
+                                                      ctypes.byref(a), _ptr(O), _ptr(N), _ptr(phase),
+                                                      ws.ptr(), ws.nbytes, _stream(stream)))
+    return O, N, phase
+
+
+def score_batch_g(store, geom, bf_idx_dev, sets, band_dev, O=None, N=None, score=None, ws=None, stream=None):
+    """score_batch() from a GStore (half plane or band copy, either format)."""
+    import torch
+    lib = load()
+    g = to_geometry(geom)
+    B = len(sets)
+    arr = (Aberr * max(B, 1))(*[to_aberr(s) for s in sets])
+    n_bf = int(bf_idx_dev.numel())
+    nq = int(band_dev.numel())
+    dev = store.G.device
+    O = torch.empty((B, nq), dtype=torch.complex64, device=dev) if O is None else O
+    N = torch.empty((B, nq), dtype=torch.int32, device=dev) if N is None else N
+    score = torch.empty((B,), dtype=torch.float64, device=dev) if score is None else score
+    if ws is None:
+        need = workspace_bytes(g, n_bf, OP_SCORE, B, nq)
+        if need == 0:
+            raise SSBError("ssb_workspace_bytes", SSB_INVALID_ARG, f"invalid sizes (B={B}, nq={nq})")
+        ws = Workspace(need, dev)
+    sc = store.c()
+    _check("ssb_score_batch_g", lib.ssb_score_batch_g(ctypes.byref(sc), ctypes.byref(g), _ptr(bf_idx_dev), n_bf,
+                                                      arr, B, _ptr(band_dev), nq, _ptr(O), _ptr(N), _ptr(score),
+                                                      ws.ptr(), ws.nbytes, _stream(stream)))
+    return O, N, score

@@ -181,18 +181,36 @@ static int check_ws(void* ws, size_t ws_bytes, size_t need) {
 }
 
 // shared by reconstruct and score: k tables, reduction, finalize
-static int run_reduction(const void* G_dev, const ssb_geometry* g, const int32_t* bf_idx, int n_bf,
+// the reductions' view of a stored G (checked); nq: band length of a
+// band-compacted copy
+static int gview_of(const ssb_gstore* s, const ssb_geometry* g, int nq, GView* v) {
+    if (!s || !s->G) return fail(SSB_INVALID_ARG, "G store or its G pointer is NULL");
+    if (s->fmt != SSB_G_C64 && s->fmt != SSB_G_SN16) return fail(SSB_INVALID_ARG, "unknown G format %d", s->fmt);
+    if (s->fmt == SSB_G_SN16) {
+        if (!s->scale) return fail(SSB_INVALID_ARG, "a herm16 G needs its scale array");
+        if (s->rows_per_scale != 1 && s->rows_per_scale != g->n)
+            return fail(SSB_UNSUPPORTED, "rows_per_scale=%d must be 1 or n=%d", s->rows_per_scale, g->n);
+    }
+    v->G = s->G;
+    v->fmt = s->fmt;
+    v->band = s->band_compact ? 1 : 0;
+    v->stride = s->band_compact ? (size_t)nq : (size_t)g->n * (g->n / 2 + 1);
+    v->scale = s->fmt == SSB_G_SN16 ? s->scale : nullptr;
+    v->srows = s->fmt == SSB_G_SN16 ? s->rows_per_scale : g->n;
+    return SSB_OK;
+}
+
+static int run_reduction(const GView& gv, const ssb_geometry* g, const int32_t* bf_idx, int n_bf,
                          const SetBatch& sb, const int32_t* qlist, int nq, float2* O, int32_t* N,
                          void* ws, const WsLayout& Lw, int want_dc, cudaStream_t st) {
     cudaError_t e;
     float4* ktab = at<float4>(ws, Lw.ktab);
     float* chik = at<float>(ws, Lw.chik);
     if ((e = launch_prep(bf_idx, n_bf, g->det_x, g->det_center_y, g->det_center_x, g->det_pitch_invA, sb,
-                         ktab, chik, static_cast<const float2*>(G_dev), (size_t)g->n * (g->n / 2 + 1),
-                         want_dc ? at<double>(ws, Lw.dcpart) : nullptr, st)) != cudaSuccess)
+                         ktab, chik, gv, want_dc ? at<double>(ws, Lw.dcpart) : nullptr, st)) != cudaSuccess)
         return cuda_fail(e, "prep");
     RedLaunch P{};
-    P.G = static_cast<const float2*>(G_dev);
+    P.g = gv;
     P.n = g->n;
     P.n_bf = n_bf;
     P.nq = nq;
@@ -393,12 +411,15 @@ int ssb_build_G_host(const void* frames_host, int dtype, const ssb_geometry* geo
                        ws_bytes - H.build, stream);
 }
 
-int ssb_reconstruct(const void* G_dev, const ssb_geometry* geom, const int32_t* bf_idx_dev, int n_bf,
-                    const ssb_aberr* set, void* O_dev, int32_t* N_dev, float* phase_dev, void* ws,
-                    size_t ws_bytes, void* stream) {
+static int reconstruct_impl(const ssb_gstore* store, const ssb_geometry* geom, const int32_t* bf_idx_dev, int n_bf,
+                            const ssb_aberr* set, void* O_dev, int32_t* N_dev, float* phase_dev, void* ws,
+                            size_t ws_bytes, void* stream) {
     int rc;
     if ((rc = check_geom(geom)) != SSB_OK) return rc;
-    if (!G_dev || !bf_idx_dev || !set || !O_dev || !N_dev || !phase_dev)
+    GView gv{};
+    if ((rc = gview_of(store, geom, 0, &gv)) != SSB_OK) return rc;
+    if (gv.band) return fail(SSB_INVALID_ARG, "a reconstruction needs the half plane, not a band-compacted G");
+    if (!bf_idx_dev || !set || !O_dev || !N_dev || !phase_dev)
         return fail(SSB_INVALID_ARG, "G, bf_idx, set, O, N and phase must not be NULL");
     if (n_bf < 1 || (long long)n_bf > (long long)geom->det_y * geom->det_x)
         return fail(SSB_INVALID_ARG, "n_bf=%d out of range", n_bf);
@@ -414,7 +435,7 @@ int ssb_reconstruct(const void* G_dev, const ssb_geometry* geom, const int32_t* 
     float2* tw = at<float2>(ws, Lw.tw);
     cudaError_t e;
     if ((e = launch_twiddles(tw, n, st)) != cudaSuccess) return cuda_fail(e, "twiddles");
-    if ((rc = run_reduction(G_dev, geom, bf_idx_dev, n_bf, sb, nullptr, nq, static_cast<float2*>(O_dev), N_dev,
+    if ((rc = run_reduction(gv, geom, bf_idx_dev, n_bf, sb, nullptr, nq, static_cast<float2*>(O_dev), N_dev,
                             ws, Lw, 1, st)) != SSB_OK)
         return rc;
     if ((e = launch_phase(static_cast<const float2*>(O_dev), N_dev, at<double>(ws, Lw.dcpart),
@@ -424,12 +445,14 @@ int ssb_reconstruct(const void* G_dev, const ssb_geometry* geom, const int32_t* 
     return SSB_OK;
 }
 
-int ssb_score_batch(const void* G_dev, const ssb_geometry* geom, const int32_t* bf_idx_dev, int n_bf,
-                    const ssb_aberr* sets, int B, const int32_t* band_dev, int nq, void* O_dev,
-                    int32_t* N_dev, double* score_dev, void* ws, size_t ws_bytes, void* stream) {
+static int score_impl(const ssb_gstore* store, const ssb_geometry* geom, const int32_t* bf_idx_dev, int n_bf,
+                      const ssb_aberr* sets, int B, const int32_t* band_dev, int nq, void* O_dev,
+                      int32_t* N_dev, double* score_dev, void* ws, size_t ws_bytes, void* stream) {
     int rc;
     if ((rc = check_geom(geom)) != SSB_OK) return rc;
-    if (!G_dev || !bf_idx_dev || !sets || !band_dev || !O_dev || !N_dev || !score_dev)
+    GView gv{};
+    if ((rc = gview_of(store, geom, nq, &gv)) != SSB_OK) return rc;
+    if (!bf_idx_dev || !sets || !band_dev || !O_dev || !N_dev || !score_dev)
         return fail(SSB_INVALID_ARG, "G, bf_idx, sets, band, O, N and score must not be NULL");
     if (B < 1 || B > SSB_MAX_SETS) return fail(SSB_UNSUPPORTED, "B=%d not in [1, %d]", B, SSB_MAX_SETS);
     if (n_bf < 1 || (long long)n_bf > (long long)geom->det_y * geom->det_x)
@@ -445,12 +468,79 @@ int ssb_score_batch(const void* G_dev, const ssb_geometry* geom, const int32_t* 
     sb.B = B;
     sb.r2 = aperture_r2(geom);
     for (int s = 0; s < B; ++s) sb.s[s] = set_params(geom, &sets[s]);
-    if ((rc = run_reduction(G_dev, geom, bf_idx_dev, n_bf, sb, band_dev, nq, static_cast<float2*>(O_dev), N_dev,
+    if ((rc = run_reduction(gv, geom, bf_idx_dev, n_bf, sb, band_dev, nq, static_cast<float2*>(O_dev), N_dev,
                             ws, Lw, 0, st)) != SSB_OK)
         return rc;
     cudaError_t e;
     if ((e = launch_score(static_cast<const float2*>(O_dev), N_dev, B, nq, score_dev, st)) != cudaSuccess)
         return cuda_fail(e, "score");
+    g_err[0] = 0;
+    return SSB_OK;
+}
+
+static ssb_gstore c64_store(const void* G_dev) {
+    ssb_gstore s{};
+    s.G = G_dev;
+    s.fmt = SSB_G_C64;
+    return s;
+}
+
+int ssb_reconstruct(const void* G_dev, const ssb_geometry* geom, const int32_t* bf_idx_dev, int n_bf,
+                    const ssb_aberr* set, void* O_dev, int32_t* N_dev, float* phase_dev, void* ws,
+                    size_t ws_bytes, void* stream) {
+    const ssb_gstore s = c64_store(G_dev);
+    return reconstruct_impl(&s, geom, bf_idx_dev, n_bf, set, O_dev, N_dev, phase_dev, ws, ws_bytes, stream);
+}
+
+int ssb_reconstruct_g(const ssb_gstore* G, const ssb_geometry* geom, const int32_t* bf_idx_dev, int n_bf,
+                      const ssb_aberr* set, void* O_dev, int32_t* N_dev, float* phase_dev, void* ws,
+                      size_t ws_bytes, void* stream) {
+    return reconstruct_impl(G, geom, bf_idx_dev, n_bf, set, O_dev, N_dev, phase_dev, ws, ws_bytes, stream);
+}
+
+int ssb_score_batch(const void* G_dev, const ssb_geometry* geom, const int32_t* bf_idx_dev, int n_bf,
+                    const ssb_aberr* sets, int B, const int32_t* band_dev, int nq, void* O_dev,
+                    int32_t* N_dev, double* score_dev, void* ws, size_t ws_bytes, void* stream) {
+    const ssb_gstore s = c64_store(G_dev);
+    return score_impl(&s, geom, bf_idx_dev, n_bf, sets, B, band_dev, nq, O_dev, N_dev, score_dev, ws, ws_bytes,
+                      stream);
+}
+
+int ssb_score_batch_g(const ssb_gstore* G, const ssb_geometry* geom, const int32_t* bf_idx_dev, int n_bf,
+                      const ssb_aberr* sets, int B, const int32_t* band_dev, int nq, void* O_dev,
+                      int32_t* N_dev, double* score_dev, void* ws, size_t ws_bytes, void* stream) {
+    return score_impl(G, geom, bf_idx_dev, n_bf, sets, B, band_dev, nq, O_dev, N_dev, score_dev, ws, ws_bytes,
+                      stream);
+}
+
+int ssb_compact_G16(const void* G_dev, const ssb_geometry* geom, int n_bf, int rows_per_scale, void* G16_dev,
+                    float* scale_dev, void* stream) {
+    int rc;
+    if ((rc = check_geom(geom)) != SSB_OK) return rc;
+    if (!G_dev || !G16_dev || !scale_dev) return fail(SSB_INVALID_ARG, "G, G16 and scale must not be NULL");
+    if (n_bf < 1) return fail(SSB_INVALID_ARG, "n_bf=%d must be >= 1", n_bf);
+    if (rows_per_scale != 1 && rows_per_scale != geom->n)
+        return fail(SSB_UNSUPPORTED, "rows_per_scale=%d must be 1 or n=%d", rows_per_scale, geom->n);
+    cudaError_t e = launch_compact_g16(static_cast<const float2*>(G_dev), geom->n, n_bf, rows_per_scale,
+                                       static_cast<uint32_t*>(G16_dev), scale_dev, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "compact_G16");
+    g_err[0] = 0;
+    return SSB_OK;
+}
+
+int ssb_compact_band(const ssb_gstore* src, const ssb_geometry* geom, int n_bf, const int32_t* band_dev, int nq,
+                     void* dst_dev, void* stream) {
+    int rc;
+    if ((rc = check_geom(geom)) != SSB_OK) return rc;
+    if (!src || !src->G || !band_dev || !dst_dev) return fail(SSB_INVALID_ARG, "G, band and dst must not be NULL");
+    if (src->fmt != SSB_G_C64 && src->fmt != SSB_G_SN16) return fail(SSB_INVALID_ARG, "unknown G format %d", src->fmt);
+    if (src->band_compact) return fail(SSB_INVALID_ARG, "the source must be a half-plane G");
+    if (n_bf < 1) return fail(SSB_INVALID_ARG, "n_bf=%d must be >= 1", n_bf);
+    if (nq < 1 || (long long)nq > (long long)geom->n * (geom->n / 2 + 1))
+        return fail(SSB_INVALID_ARG, "nq=%d out of range", nq);
+    cudaError_t e = launch_compact_band(src->G, src->fmt, (size_t)geom->n * (geom->n / 2 + 1), n_bf, band_dev, nq,
+                                        dst_dev, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "compact_band");
     g_err[0] = 0;
     return SSB_OK;
 }

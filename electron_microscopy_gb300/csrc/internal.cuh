@@ -350,8 +350,30 @@ cudaError_t launch_build512(const uint16_t* frames, int det_pix, const int32_t* 
 // in chik[k * kChiStride + s]
 constexpr int kChiStride = 8;
 
+// a stored G as the reductions read it: complex64 entries, or herm16 words
+// (two int16 codes, real in the low half) with float32 scales
+// [n / srows][n_bf]; entry (k, i) sits at k * stride + i, i the half-plane
+// entry or, for a band-compacted copy, the band position
+enum GFormat { kGC64 = 0, kGSN16 = 1 };
+struct GView {
+    const void* G;
+    int fmt;
+    size_t stride;          // entries between consecutive BF pixels
+    int band;               // 1: indexed by band position, not half-plane entry
+    const float* scale;     // kGSN16
+    int srows;              // kGSN16: q rows per scale block (1 or n)
+};
+
+// one herm16 word to complex64: max(code, -32767) * s, s = scale * (1/32767)
+__device__ __forceinline__ float2 sn16_unpack(uint32_t w, float s) {
+    const int re = max((int)(int16_t)(w & 0xffffu), -32767);
+    const int im = max((int)(int16_t)(w >> 16), -32767);
+    return make_float2(__fmul_rn((float)re, s), __fmul_rn((float)im, s));
+}
+constexpr float kInv32767 = 1.0f / 32767.0f;
+
 struct RedLaunch {
-    const float2* G;
+    GView g;
     int n, n_bf, nq, nsplit, kps;
     double dq;
     const int32_t* qlist;   // null: identity over the half plane
@@ -363,8 +385,9 @@ struct RedLaunch {
 };
 
 // dcpart (may be null): per-256-pixel-block sums of Re G(0,k) in float64
+// (G must then be a half plane: entry 0 is q = 0)
 cudaError_t launch_prep(const int32_t* bf_idx, int n_bf, int det_x, double cy, double cx, double dk,
-                        const SetBatch& sb, float4* ktab, float* chik, const float2* G, size_t plane,
+                        const SetBatch& sb, float4* ktab, float* chik, const GView& g,
                         double* dcpart, cudaStream_t st);
 cudaError_t launch_reduce(const RedLaunch& L, const SetBatch& sb, cudaStream_t st);
 cudaError_t launch_finalize(const float2* Opart, const int* Npart, int nsplit, int B, int nq,
@@ -374,6 +397,11 @@ cudaError_t launch_phase(const float2* O, const int32_t* N, const double* dcpart
                          cudaStream_t st);
 cudaError_t launch_score(const float2* O, const int32_t* N, int B, int nq, double* score,
                          cudaStream_t st);
+// compact storage (compact.cu)
+cudaError_t launch_compact_g16(const float2* G, int n, int n_bf, int srows, uint32_t* G16, float* scale,
+                               cudaStream_t st);
+cudaError_t launch_compact_band(const void* G, int fmt, size_t plane, int n_bf, const int32_t* band, int nq,
+                                void* dst, cudaStream_t st);
 
 // launch bookkeeping (api.cu)
 void count_launch(int k = 1);

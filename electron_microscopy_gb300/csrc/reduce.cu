@@ -31,14 +31,22 @@ namespace ssb {
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256)
 ssb_prep(const int32_t* __restrict__ bf_idx, int n_bf, int det_x, double cy, double cx, double dk, SetBatch sb,
-         float4* __restrict__ ktab, float* __restrict__ chik, const float2* __restrict__ G, size_t plane,
-         double* __restrict__ dcpart) {
+         float4* __restrict__ ktab, float* __restrict__ chik, GView g, double* __restrict__ dcpart) {
     const int k = blockIdx.x * blockDim.x + threadIdx.x;
     if (dcpart) {
         // sum_k Re G(0, k) for the image offset a: per-block partial in
-        // float64, added in a fixed order by the image kernel
+        // float64, added in a fixed order by the image kernel (entry 0 of a
+        // half plane is q = 0, in the scale block of row 0)
         __shared__ double red[256];
-        red[threadIdx.x] = k < n_bf ? (double)G[(size_t)k * plane].x : 0.0;
+        float g0 = 0.f;
+        if (k < n_bf) {
+            if (g.fmt == kGSN16)
+                g0 = sn16_unpack(static_cast<const uint32_t*>(g.G)[(size_t)k * g.stride],
+                                 __fmul_rn(g.scale[k], kInv32767)).x;
+            else
+                g0 = static_cast<const float2*>(g.G)[(size_t)k * g.stride].x;
+        }
+        red[threadIdx.x] = (double)g0;
         __syncthreads();
         for (int w = 128; w > 0; w >>= 1) {
             if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
@@ -68,9 +76,9 @@ ssb_prep(const int32_t* __restrict__ bf_idx, int n_bf, int det_x, double cy, dou
 }
 
 cudaError_t launch_prep(const int32_t* bf_idx, int n_bf, int det_x, double cy, double cx, double dk,
-                        const SetBatch& sb, float4* ktab, float* chik, const float2* G, size_t plane,
+                        const SetBatch& sb, float4* ktab, float* chik, const GView& g,
                         double* dcpart, cudaStream_t st) {
-    ssb_prep<<<(n_bf + 255) / 256, 256, 0, st>>>(bf_idx, n_bf, det_x, cy, cx, dk, sb, ktab, chik, G, plane, dcpart);
+    ssb_prep<<<(n_bf + 255) / 256, 256, 0, st>>>(bf_idx, n_bf, det_x, cy, cx, dk, sb, ktab, chik, g, dcpart);
     count_launch();
     return cudaGetLastError();
 }
@@ -122,7 +130,7 @@ constexpr size_t red_smem_bytes() {
 template <int MAXB, bool SHARED>
 __host__ __device__ constexpr int red_min_blocks() { return (MAXB == 1 || SHARED) ? 4 : 2; }
 
-template <int MAXB, bool SHARED>
+template <int MAXB, bool SHARED, int FMT>
 __global__ void __launch_bounds__(kRedThreads, red_min_blocks<MAXB, SHARED>())
 ssb_reduce(RedLaunch P, SetBatch sb) {
     const int qi = blockIdx.x * kRedThreads + threadIdx.x;
@@ -144,8 +152,14 @@ ssb_reduce(RedLaunch P, SetBatch sb) {
         acc[s] = make_float2(0.f, 0.f);
         cnt[s] = 0;
     }
-    const size_t plane = (size_t)P.n * H;
-    const float2* gp = P.G + e;
+    // this lane's G entry of pixel k sits at k * gstride + gi: the half-plane
+    // entry, or the band position in a band-compacted copy; herm16 scales of
+    // the lane's q row (one scale per pixel: block 0)
+    const size_t gstride = P.g.stride;
+    const size_t gi = valid ? (P.g.band ? (size_t)qi : (size_t)e) : 0;
+    const float2* gp = static_cast<const float2*>(P.g.G) + gi;
+    const uint32_t* gw = static_cast<const uint32_t*>(P.g.G) + gi;
+    const float* gsc = P.g.scale + (FMT == kGSN16 && P.g.srows == 1 ? (size_t)row * P.n_bf : 0);
 
     // chi(k -/+ q) along the current detector row: per trotter side and set,
     // the coefficients of chi as a quartic in vx (vy is fixed along a row at
@@ -275,20 +289,38 @@ ssb_reduce(RedLaunch P, SetBatch sb) {
     __shared__ float4 s_chik[MAXB > 1 ? kKChunk * kChiStride / 4 : 1];
     auto walk = [&](auto tab, int kc0, int kcn) {
         constexpr int U = red_unroll<MAXB>();
-        const float2* gk = gp + (size_t)kc0 * plane;
+        [[maybe_unused]] const float2* gk = gp + (size_t)kc0 * gstride;
+        [[maybe_unused]] const uint32_t* wk = gw + (size_t)kc0 * gstride;
+        [[maybe_unused]] const float* sk = gsc + kc0;
         int i = 0;
 #pragma unroll 1
         for (; i + U <= kcn; i += U) {
             float2 g[U];
+            if constexpr (FMT == kGC64) {
 #pragma unroll
-            for (int u = 0; u < U; ++u) g[u] = valid ? __ldcs(gk + (size_t)(i + u) * plane) : make_float2(0.f, 0.f);
+                for (int u = 0; u < U; ++u)
+                    g[u] = valid ? __ldcs(gk + (size_t)(i + u) * gstride) : make_float2(0.f, 0.f);
+            } else {
+                uint32_t w[U];
+                float sc[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) w[u] = valid ? __ldcs(wk + (size_t)(i + u) * gstride) : 0u;
+#pragma unroll
+                for (int u = 0; u < U; ++u) sc[u] = __ldg(sk + i + u);
+#pragma unroll
+                for (int u = 0; u < U; ++u) g[u] = sn16_unpack(w[u], __fmul_rn(sc[u], kInv32767));
+            }
 #pragma unroll
             for (int u = 0; u < U; ++u)
                 step(g[u], s_ktab[i + u], reinterpret_cast<const float*>(s_chik) + (i + u) * kChiStride, tab);
         }
 #pragma unroll 1
         for (; i < kcn; ++i) {
-            const float2 g = valid ? __ldcs(gk + (size_t)i * plane) : make_float2(0.f, 0.f);
+            float2 g;
+            if constexpr (FMT == kGC64)
+                g = valid ? __ldcs(gk + (size_t)i * gstride) : make_float2(0.f, 0.f);
+            else
+                g = sn16_unpack(valid ? __ldcs(wk + (size_t)i * gstride) : 0u, __fmul_rn(__ldg(sk + i), kInv32767));
             step(g, s_ktab[i], reinterpret_cast<const float*>(s_chik) + i * kChiStride, tab);
         }
     };
@@ -319,37 +351,46 @@ ssb_reduce(RedLaunch P, SetBatch sb) {
     }
 }
 
-template <int MAXB, bool SHARED>
-static void launch_reduce_bs(const RedLaunch& P, const SetBatch& sb, dim3 grid, cudaStream_t st) {
+template <int MAXB, bool SHARED, int FMT>
+static void launch_reduce_bsf(const RedLaunch& P, const SetBatch& sb, dim3 grid, cudaStream_t st) {
     constexpr size_t smem = red_smem_bytes<MAXB>();
     if (smem > 48 * 1024) {
         static bool opted = false;  // idempotent attribute; a racing second set is harmless
         if (!opted) {
-            cudaFuncSetAttribute(ssb_reduce<MAXB, SHARED>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            cudaFuncSetAttribute(ssb_reduce<MAXB, SHARED, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
             opted = true;
         }
     }
-    ssb_reduce<MAXB, SHARED><<<grid, kRedThreads, smem, st>>>(P, sb);
+    ssb_reduce<MAXB, SHARED, FMT><<<grid, kRedThreads, smem, st>>>(P, sb);
 }
 
-template <int MAXB>
-static void launch_reduce_b(const RedLaunch& P, const SetBatch& sb, dim3 grid, cudaStream_t st) {
+template <int MAXB, int FMT>
+static void launch_reduce_bf(const RedLaunch& P, const SetBatch& sb, dim3 grid, cudaStream_t st) {
     if (P.shared_tilt)
-        launch_reduce_bs<MAXB, true>(P, sb, grid, st);
+        launch_reduce_bsf<MAXB, true, FMT>(P, sb, grid, st);
     else
-        launch_reduce_bs<MAXB, false>(P, sb, grid, st);
+        launch_reduce_bsf<MAXB, false, FMT>(P, sb, grid, st);
+}
+
+template <int FMT>
+static void launch_reduce_f(const RedLaunch& P, const SetBatch& sb, dim3 grid, cudaStream_t st) {
+    if (sb.B == 1)
+        launch_reduce_bf<1, FMT>(P, sb, grid, st);
+    else if (sb.B == 2)
+        launch_reduce_bf<2, FMT>(P, sb, grid, st);
+    else if (sb.B <= 4)
+        launch_reduce_bf<4, FMT>(P, sb, grid, st);
+    else
+        launch_reduce_bf<8, FMT>(P, sb, grid, st);
 }
 
 cudaError_t launch_reduce(const RedLaunch& P, const SetBatch& sb, cudaStream_t st) {
     dim3 grid((P.nq + kRedThreads - 1) / kRedThreads, P.nsplit);
-    if (sb.B == 1)
-        launch_reduce_b<1>(P, sb, grid, st);
-    else if (sb.B == 2)
-        launch_reduce_b<2>(P, sb, grid, st);
-    else if (sb.B <= 4)
-        launch_reduce_b<4>(P, sb, grid, st);
+    if (P.g.fmt == kGSN16)
+        launch_reduce_f<kGSN16>(P, sb, grid, st);
     else
-        launch_reduce_b<8>(P, sb, grid, st);
+        launch_reduce_f<kGC64>(P, sb, grid, st);
     count_launch();
     return cudaGetLastError();
 }

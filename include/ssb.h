@@ -210,6 +210,86 @@ int ssb_score_batch(const void* G_dev, const ssb_geometry* geom,
                     void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Compact storage of G.
+ *
+ * herm16 (source: "Historical WebGPU G(q,k) memory experiment", sections
+ * "Implementation", "Memory planning table" and "Scan-size sweep"): each
+ * half-plane entry is one 32-bit word holding two 16-bit two's complement
+ * codes, the real part in bits 0-15 and the imaginary part in bits 16-31,
+ *   code = floor(0.5 + 32767 * clamp(v / scale, -1, 1)),
+ * every operation a separately rounded float32 operation, with scale the
+ * largest |G| (float32 sqrt of the float32 re*re + im*im) over a block of the
+ * pixel's half plane: the whole plane (rows_per_scale = n, the page's preview
+ * form, 4 bytes per BF pixel) or one q row (rows_per_scale = 1, the page's
+ * follow-up, n scales per BF pixel).  A block whose largest |G| is 0 has scale
+ * 0 and codes 0.  Scales are float32 [n / rows_per_scale][n_bf] (block-major).
+ * A reader takes max(code, -32767) * (scale * (1/32767)) in float32.
+ *
+ * Band-compacted copy (no page describes it; the scoring passes of a fit read
+ * only the band, 78 passes per fit in "Tilt-corrected SSB on CUDA", section
+ * "Where the time went"): entry i of row k is the half-plane entry band[i] of
+ * BF pixel k, [n_bf][nq], in either element format.  herm16 scales are not
+ * copied: the band entry's q row still selects the scale.
+ */
+typedef enum ssb_gfmt { SSB_G_C64 = 0, SSB_G_SN16 = 1 } ssb_gfmt;
+
+/* A stored G as the reductions read it (every pointer device memory). */
+typedef struct ssb_gstore {
+    const void* G;          /* complex64 (SSB_G_C64) or herm16 words (SSB_G_SN16)        */
+    int fmt;                /* ssb_gfmt                                                   */
+    const float* scale;     /* SSB_G_SN16: [n / rows_per_scale][n_bf]; else ignored       */
+    int rows_per_scale;     /* SSB_G_SN16: 1 or n; else ignored                           */
+    int band_compact;       /* 0: [n_bf][n][n/2+1] half planes; 1: [n_bf][nq] band copy   */
+} ssb_gstore;
+
+/*
+ * herm16 from a complex64 G (G_dev: [n_bf][n][n/2+1]).  Writes G16_dev (uint32
+ * [n_bf][n][n/2+1]) and scale_dev (float32 [n / rows_per_scale][n_bf]); the
+ * outputs must not overlap G_dev.  Deterministic: the codes and scales are a
+ * function of G alone (bit for bit).  Errors: SSB_INVALID_ARG for a null
+ * pointer or n_bf < 1, SSB_UNSUPPORTED for rows_per_scale not in {1, n}.
+ */
+int ssb_compact_G16(const void* G_dev, const ssb_geometry* geom, int n_bf, int rows_per_scale,
+                    void* G16_dev, float* scale_dev, void* stream);
+
+/*
+ * Band-compacted copy of a half-plane G (src->band_compact must be 0; only
+ * src->G and src->fmt are read): dst_dev[k][i] = G[k][band[i]], 8-byte entries
+ * for SSB_G_C64, 4-byte words for SSB_G_SN16.  band_dev: device int32[nq] of
+ * half-plane entries (as ssb_band_indices writes them).  Bit-exact copy.
+ * Errors: SSB_INVALID_ARG for a null pointer, n_bf < 1, nq out of
+ * [1, n*(n/2+1)], an unknown format or a band-compacted source.
+ */
+int ssb_compact_band(const ssb_gstore* src, const ssb_geometry* geom, int n_bf, const int32_t* band_dev,
+                     int nq, void* dst_dev, void* stream);
+
+/*
+ * ssb_reconstruct from any stored G (G: host pointer to the descriptor; the
+ * half plane is needed, so G->band_compact must be 0).  With SSB_G_C64 this is
+ * ssb_reconstruct bit for bit.  Errors as ssb_reconstruct, plus
+ * SSB_INVALID_ARG for a band-compacted G, a missing scale array or an unknown
+ * format, SSB_UNSUPPORTED for rows_per_scale not in {1, n}.
+ */
+int ssb_reconstruct_g(const ssb_gstore* G, const ssb_geometry* geom,
+                      const int32_t* bf_idx_dev, int n_bf, const ssb_aberr* set,
+                      void* O_dev, int32_t* N_dev, float* phase_dev,
+                      void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * ssb_score_batch from any stored G.  A band-compacted G must come from the
+ * same band_dev and nq.  Every (G format, layout) gives, per set, the same
+ * arithmetic in the same order as ssb_score_batch on the G it stores, so a
+ * band-compacted complex64 copy scores bit for bit like the half plane.
+ * Errors as ssb_score_batch, plus those of ssb_reconstruct_g for the
+ * descriptor.
+ */
+int ssb_score_batch_g(const ssb_gstore* G, const ssb_geometry* geom,
+                      const int32_t* bf_idx_dev, int n_bf, const ssb_aberr* sets, int B,
+                      const int32_t* band_dev, int nq,
+                      void* O_dev, int32_t* N_dev, double* score_dev,
+                      void* ws, size_t ws_bytes, void* stream);
+
+/*
  * ssb_reconstruct for callers that cannot allocate device memory.
  *
  * No page describes this call; it has no counterpart in the method.  It exists

@@ -202,3 +202,49 @@ def test_error_codes_build_host(lib):
     rc = lib.ssb_build_G_host(FAKE, 0, ctypes.byref(_g(n=100)), bfp, FAKE, 3, FAKE, FAKE, big, None)
     assert rc == ssb.SSB_UNSUPPORTED
     assert lib.ssb_launch_count() == before
+
+
+def test_error_codes_compact_storage(lib):
+    """The compact-storage entry points and the G descriptor are checked on
+    the host and rejected before anything is launched."""
+    g = _g()  # n = 32
+    before = lib.ssb_launch_count()
+    S = ssb.GStoreC
+    big = 1 << 30
+    # ssb_compact_G16
+    assert lib.ssb_compact_G16(None, ctypes.byref(g), 10, 1, FAKE, FAKE, None) == ssb.SSB_INVALID_ARG
+    assert lib.ssb_compact_G16(FAKE, ctypes.byref(g), 0, 1, FAKE, FAKE, None) == ssb.SSB_INVALID_ARG
+    assert lib.ssb_compact_G16(FAKE, ctypes.byref(g), 10, 1, FAKE, None, None) == ssb.SSB_INVALID_ARG
+    for rows in (0, 2, 16, 64):
+        assert lib.ssb_compact_G16(FAKE, ctypes.byref(g), 10, rows, FAKE, FAKE, None) == ssb.SSB_UNSUPPORTED, rows
+    # ssb_compact_band
+    src = S(FAKE.value, ssb.G_C64, 0, 0, 0)
+    assert lib.ssb_compact_band(None, ctypes.byref(g), 10, FAKE, 5, FAKE, None) == ssb.SSB_INVALID_ARG
+    assert lib.ssb_compact_band(ctypes.byref(src), ctypes.byref(g), 10, FAKE, 0, FAKE, None) == ssb.SSB_INVALID_ARG
+    assert lib.ssb_compact_band(ctypes.byref(src), ctypes.byref(g), 10, FAKE, 32 * 17 + 1, FAKE,
+                                None) == ssb.SSB_INVALID_ARG
+    assert lib.ssb_compact_band(ctypes.byref(src), ctypes.byref(g), 0, FAKE, 5, FAKE, None) == ssb.SSB_INVALID_ARG
+    bad = S(FAKE.value, 7, 0, 0, 0)
+    assert lib.ssb_compact_band(ctypes.byref(bad), ctypes.byref(g), 10, FAKE, 5, FAKE, None) == ssb.SSB_INVALID_ARG
+    banded = S(FAKE.value, ssb.G_C64, 0, 0, 1)
+    assert lib.ssb_compact_band(ctypes.byref(banded), ctypes.byref(g), 10, FAKE, 5, FAKE,
+                                None) == ssb.SSB_INVALID_ARG
+    # descriptors the reductions reject
+    a = ssb.Aberr()
+    sets = (ssb.Aberr * 2)()
+    no_scale = S(FAKE.value, ssb.G_SN16, 0, 1, 0)
+    odd_rows = S(FAKE.value, ssb.G_SN16, FAKE.value, 4, 0)
+    for store, code in ((bad, ssb.SSB_INVALID_ARG), (no_scale, ssb.SSB_INVALID_ARG),
+                        (odd_rows, ssb.SSB_UNSUPPORTED)):
+        rc = lib.ssb_reconstruct_g(ctypes.byref(store), ctypes.byref(g), FAKE, 10, ctypes.byref(a), FAKE, FAKE,
+                                   FAKE, FAKE, big, None)
+        assert rc == code
+        rc = lib.ssb_score_batch_g(ctypes.byref(store), ctypes.byref(g), FAKE, 10, sets, 2, FAKE, 5, FAKE, FAKE,
+                                   FAKE, FAKE, big, None)
+        assert rc == code
+    rc = lib.ssb_reconstruct_g(ctypes.byref(banded), ctypes.byref(g), FAKE, 10, ctypes.byref(a), FAKE, FAKE, FAKE,
+                               FAKE, big, None)
+    assert rc == ssb.SSB_INVALID_ARG
+    assert lib.ssb_reconstruct_g(None, ctypes.byref(g), FAKE, 10, ctypes.byref(a), FAKE, FAKE, FAKE, FAKE, big,
+                                 None) == ssb.SSB_INVALID_ARG
+    assert lib.ssb_launch_count() == before
