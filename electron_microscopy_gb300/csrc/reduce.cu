@@ -212,7 +212,16 @@ ssb_reduce(RedLaunch P, SetBatch sb) {
         }
     };
 
-    auto step = [&](float2 g, float4 kd, const float* chk, auto tab) {
+    // a k step's G: complex64 as loaded, or (herm16 word, scale bits),
+    // dequantised only inside the branches that accumulate a term
+    using GIn = std::conditional_t<FMT == kGC64, float2, uint2>;
+    auto gval = [&](const GIn& gi) -> float2 {
+        if constexpr (FMT == kGC64)
+            return gi;
+        else
+            return sn16_unpack(gi.x, __fmul_rn(__uint_as_float(gi.y), kInv32767));
+    };
+    auto step = [&](const GIn& g, float4 kd, const float* chk, auto tab) {
         if (decltype(tab)::value && kd.y != cur_ky) {  // uniform: every lane walks the same k
             new_row(kd.y);
             cur_ky = kd.y;
@@ -233,7 +242,8 @@ ssb_reduce(RedLaunch P, SetBatch sb) {
                 // inactive lanes add an exact zero: gs = 0 * G, and every
                 // later term is finite
                 const float sg = act ? (m ? 1.0f : -1.0f) : 0.0f;
-                accumulate(acc[0], make_float2(__fmul_rn(sg, g.x), __fmul_rn(sg, g.y)), kd.w,
+                const float2 gv = gval(g);
+                accumulate(acc[0], make_float2(__fmul_rn(sg, gv.x), __fmul_rn(sg, gv.y)), kd.w,
                            chi_v(tab, 0, m, m ? mvx : pvx, 0.f), m ? kTwoPi : -kTwoPi);
                 cnt[0] += act ? 1 : 0;
             }
@@ -246,7 +256,7 @@ ssb_reduce(RedLaunch P, SetBatch sb) {
                 const bool p = aperture_f32(px, py, sb.s[0].tx, sb.s[0].ty, sb.r2, &pvx, &pvy);
                 if (m != p) {
                     const float x = m ? mvx : pvx, y = m ? mvy : pvy;
-                    const float2 gs = side_sign(g, m);
+                    const float2 gs = side_sign(gval(g), m);
                     const float tw = m ? kTwoPi : -kTwoPi;
                     cnt[0] += 1;
                     float ck[MAXB];
@@ -273,7 +283,7 @@ ssb_reduce(RedLaunch P, SetBatch sb) {
                     const bool p = aperture_f32(px, py, sb.s[s].tx, sb.s[s].ty, sb.r2, &pvx, &pvy);
                     if (m != p) {
                         const float cq = chi_v(tab, s, m, m ? mvx : pvx, m ? mvy : pvy);
-                        accumulate(acc[s], side_sign(g, m), chk[s], cq,
+                        accumulate(acc[s], side_sign(gval(g), m), chk[s], cq,
                                    m ? kTwoPi : -kTwoPi);
                         cnt[s] += 1;
                     }
@@ -295,20 +305,16 @@ ssb_reduce(RedLaunch P, SetBatch sb) {
         int i = 0;
 #pragma unroll 1
         for (; i + U <= kcn; i += U) {
-            float2 g[U];
+            GIn g[U];
             if constexpr (FMT == kGC64) {
 #pragma unroll
                 for (int u = 0; u < U; ++u)
                     g[u] = valid ? __ldcs(gk + (size_t)(i + u) * gstride) : make_float2(0.f, 0.f);
             } else {
-                uint32_t w[U];
-                float sc[U];
 #pragma unroll
-                for (int u = 0; u < U; ++u) w[u] = valid ? __ldcs(wk + (size_t)(i + u) * gstride) : 0u;
+                for (int u = 0; u < U; ++u) g[u].x = valid ? __ldcs(wk + (size_t)(i + u) * gstride) : 0u;
 #pragma unroll
-                for (int u = 0; u < U; ++u) sc[u] = __ldg(sk + i + u);
-#pragma unroll
-                for (int u = 0; u < U; ++u) g[u] = sn16_unpack(w[u], __fmul_rn(sc[u], kInv32767));
+                for (int u = 0; u < U; ++u) g[u].y = __float_as_uint(__ldg(sk + i + u));
             }
 #pragma unroll
             for (int u = 0; u < U; ++u)
@@ -316,11 +322,11 @@ ssb_reduce(RedLaunch P, SetBatch sb) {
         }
 #pragma unroll 1
         for (; i < kcn; ++i) {
-            float2 g;
+            GIn g;
             if constexpr (FMT == kGC64)
                 g = valid ? __ldcs(gk + (size_t)i * gstride) : make_float2(0.f, 0.f);
             else
-                g = sn16_unpack(valid ? __ldcs(wk + (size_t)i * gstride) : 0u, __fmul_rn(__ldg(sk + i), kInv32767));
+                g = make_uint2(valid ? __ldcs(wk + (size_t)i * gstride) : 0u, __float_as_uint(__ldg(sk + i)));
             step(g, s_ktab[i], reinterpret_cast<const float*>(s_chik) + i * kChiStride, tab);
         }
     };
