@@ -453,3 +453,73 @@ def band_compact(G, band):
     G = np.asarray(G)
     nbf, n, h = G.shape[:3]
     return G.reshape((nbf, n * h) + G.shape[3:])[:, np.asarray(band, dtype=np.int64)]
+
+
+# ----------------------------------------------------------------------------
+# per-BF phase moments: the exact mean(angle) path
+# ----------------------------------------------------------------------------
+# Sources: "Historical WebGPU G(q,k) memory experiment", section "Object-redraw
+# fast path": the exact per-BF path takes, for every BF pixel, the inverse FFT
+# of its aberration-corrected plane and the angle of that object, and averages
+# the angles (mean(angle(object))); the loss needs the per-BF phases because it
+# uses the variance of mean(angle).  "Tilt-corrected SSB on CUDA", sections
+# "Changes" (Loss path: the corrected plane is written from the stored half
+# plane, the angles are reduced to moments as they are read) and "Open" (the
+# corrected spectrum of a real image is anti-Hermitian except at DC, so a
+# half-plane complex-to-real transform gives the image).
+#
+# READING corrected plane: S_k(q) = G(q,k) w(q,k) on the trotter pixels of BF
+# pixel k (the terms the reduction sums), 0 elsewhere; zeroed at DC and on the
+# Nyquist row and column as in the single image.
+# READING object of one BF pixel: a_k + i b_k with a_k = Re G(0,k) / n^2 and
+# b_k = irfft2(-i S_k) (numpy semantics), the per-pixel form of the image's
+# a + i b; its angle is atan2(b_k, a_k).
+# READING moments: per scan pixel, the mean over the N_bf BF pixels of the
+# angle and its population variance (divided by N_bf).  The pages give no
+# scalar loss formula, so the moments are the output.
+
+
+def corrected_planes(G, geom, ab, bf_idx, chunk=512):
+    """S_k(q) = G(q,k) w(q,k) on T-(q) | T+(q) of pixel k, 0 elsewhere:
+    complex128 (N_bf, n, n/2+1)."""
+    nbf, n, h = G.shape
+    qx_col, qy_row = q_coords(geom)
+    Gf = np.asarray(G).reshape(nbf, n * h)
+    S = np.zeros((nbf, n * h), dtype=np.complex128)
+    for s in range(0, n * h, chunk):
+        e = np.arange(s, min(s + chunk, n * h))
+        qx = qx_col[e % h]
+        qy = qy_row[e // h]
+        tm, tp = trotters(geom, ab, bf_idx, qx, qy)
+        w = weights(geom, ab, bf_idx, qx, qy, tm, tp)          # (chunk, N_bf), 0 off the trotters
+        S[:, e] = Gf[:, e] * w.T
+    return S.reshape(nbf, n, h)
+
+
+def per_bf_images(G, geom, ab, bf_idx):
+    """(a_k, b_k) of every BF pixel in order: a_k = Re G(0,k) / n^2 (float),
+    b_k = irfft2(-i S_k) (float64 (n, n)) with S_k zeroed at DC and on the
+    Nyquist row and column."""
+    nbf, n, h = G.shape
+    S = corrected_planes(G, geom, ab, bf_idx)
+    for k in range(nbf):
+        Sk = S[k].copy()
+        Sk[n // 2, :] = 0.0
+        Sk[:, n // 2] = 0.0
+        Sk[0, 0] = 0.0
+        yield float(np.real(G[k, 0, 0])) / (n * n), np.fft.irfft2(-1j * Sk, s=(n, n))
+
+
+def phase_moments(G, geom, ab, bf_idx):
+    """Per scan pixel: mean over BF pixels of atan2(b_k, a_k) and its
+    population variance.  Returns (mean, var), float64 (n, n)."""
+    nbf, n, _ = G.shape
+    s1 = np.zeros((n, n))
+    s2 = np.zeros((n, n))
+    for a, b in per_bf_images(G, geom, ab, bf_idx):
+        ph = np.arctan2(b, a)
+        s1 += ph
+        s2 += ph * ph
+    mean = s1 / nbf
+    var = np.maximum(s2 / nbf - mean * mean, 0.0)
+    return mean, var

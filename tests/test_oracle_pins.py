@@ -390,3 +390,94 @@ def test_band_membership_integer_rule():
     allq = np.hypot(fy[:, None] * dq, fx[None, :] * dq).ravel()
     inside = np.flatnonzero((allq > 0.2 + 1e-9) & (allq < 0.9 - 1e-9))
     assert set(inside).issubset(set(band))
+
+
+# ----------------------------------------------------------------------------
+# per-BF phase moments (the exact mean(angle) path)
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("fy0,fx0", [(-3, 5), (4, 0)])
+def test_phase_moments_single_cosine_closed_form(fy0, fx0):
+    """Linear intensities of phi = eps cos(2 pi q0.r): S_k(q0) = i eps/2 n^2
+    on every trotter pixel of q0 and 0 on the others, a_k = 1, so phase_k =
+    atan(eps cos) on a fraction f = N(q0) / N_bf of the pixels and 0 on the
+    rest: mean = f atan(eps cos), variance = f (1 - f) atan(eps cos)^2."""
+    g = _geom(n=32, det=28, dk=0.17)
+    ab = _ab(C10=-80.0, C12a=20.0, C12b=-15.0, C21a=30.0, C23b=-25.0, C30=5e3,
+             C32a=-2e3, C34b=3e3, tilt_x_rad=3e-3, tilt_y_rad=-1.5e-3)
+    eps = 0.05
+    bf = O.bf_indices(g, ab.tilt_x_rad, ab.tilt_y_rad)
+    inten, _ = _linear_intensity_single_cosine(g, ab, bf, eps, fy0, fx0)
+    G = O.build_G(inten, bf)
+    n, h = g.n, g.n // 2 + 1
+    _, Nq = O.reduce(G, g, ab, bf, entries=np.array([(fy0 % n) * h + fx0]))
+    f = Nq[0] / len(bf)
+    assert 0 < f < 1
+    mean, var = O.phase_moments(G, g, ab, bf)
+    ry, rx = np.meshgrid(np.arange(n), np.arange(n), indexing="ij")
+    t = np.arctan(eps * np.cos(2 * math.pi * (fy0 * ry + fx0 * rx) / n))
+    assert np.abs(mean - f * t).max() < 1e-12
+    assert np.abs(var - f * (1 - f) * t * t).max() < 1e-12
+
+
+def test_per_bf_image_matches_bruteforce_inverse_dft():
+    """b_k against an explicit inverse DFT over the full plane, the other half
+    filled by S(-q) = -conj S(q) (anti-Hermitian corrected spectrum)."""
+    rng = np.random.default_rng(21)
+    n, det = 8, 10
+    g = _geom(n=n, det=det, dk=0.45)
+    ab = _ab(C10=-30.0, C12a=8.0, C21b=20.0, C30=4e3, tilt_x_rad=2e-3)
+    frames = rng.uniform(0, 30, size=(n, n, det, det))
+    bf = O.bf_indices(g, ab.tilt_x_rad, ab.tilt_y_rad)[:6]
+    G = O.build_G(frames, bf)
+    S = O.corrected_planes(G, g, ab, bf)
+    h = n // 2 + 1
+    ry, rx = np.meshgrid(np.arange(n), np.arange(n), indexing="ij")
+    for k, (a, b) in enumerate(O.per_bf_images(G, g, ab, bf)):
+        assert a == G[k, 0, 0].real / (n * n)
+        ref = np.zeros((n, n))
+        for fy in range(-n // 2, n // 2):
+            for fx in range(-n // 2, n // 2):
+                if fy == -n // 2 or fx == -n // 2 or (fy == 0 and fx == 0):
+                    continue  # Nyquist row and column, DC: zeroed
+                if fx >= 0:
+                    s = S[k, fy % n, fx]
+                else:
+                    s = -np.conj(S[k, (-fy) % n, -fx])
+                ref += np.real(-1j * s * np.exp(2j * math.pi * (fy * ry + fx * rx) / n))
+        ref /= n * n
+        assert np.abs(b - ref).max() < 1e-12 * max(1.0, np.abs(ref).max())
+
+
+def test_per_bf_mean_of_objects_is_the_fast_path():
+    """The pages' identity mean_k ifft2(corrected_k) = ifft2(mean_k corrected_k):
+    atan2(mean b_k, mean a_k) equals the single image with the BF-mean
+    normalisation (O / N_bf), an independent route through the reduction."""
+    rng = np.random.default_rng(22)
+    n, det = 16, 14
+    g = _geom(n=n, det=det, dk=0.3)
+    ab = _ab(C10=-50.0, C12b=10.0, C23a=15.0, C30=2e3, tilt_y_rad=1e-3)
+    frames = rng.uniform(0, 30, size=(n, n, det, det))
+    bf = O.bf_indices(g, ab.tilt_x_rad, ab.tilt_y_rad)
+    G = O.build_G(frames, bf)
+    sa, sb = 0.0, np.zeros((n, n))
+    for a, b in O.per_bf_images(G, g, ab, bf):
+        sa += a
+        sb += b
+    Oq, Nq = O.reduce(G, g, ab, bf)
+    fast = O.phase_image(Oq, Nq, O.g0_mean(G), n, norm="bf_mean", n_bf=len(bf))
+    assert np.abs(np.arctan2(sb / len(bf), sa / len(bf)) - fast).max() < 1e-12
+
+
+def test_phase_moments_of_one_pixel():
+    rng = np.random.default_rng(23)
+    n, det = 16, 12
+    g = _geom(n=n, det=det, dk=0.3)
+    ab = _ab(C10=-20.0, C30=1e3)
+    frames = rng.uniform(0, 30, size=(n, n, det, det))
+    bf = O.bf_indices(g)[5:6]
+    G = O.build_G(frames, bf)
+    mean, var = O.phase_moments(G, g, ab, bf)
+    (a, b), = list(O.per_bf_images(G, g, ab, bf))
+    assert np.array_equal(mean, np.arctan2(b, a))
+    assert var.max() < 1e-15
