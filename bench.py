@@ -550,6 +550,19 @@ def run_ours(args, ws, rank, local, pg):
                 "recon_hbm_frac": rec_bytes / (t_rec * 1e-3) / 1e9 / hbm, "recon_algorithmic_bytes": rec_bytes,
                 "band_score_sweep": sweep(ssb.GStore(Wb, ssb.G_SN16, S, rows, band_compact=True), bb16)}
             del W, S, Wb, st
+        # per-BF phase moments (the exact mean(angle) path) from the complex64
+        # half plane: G read once, every corrected plane through L2
+        mom_mean = torch.empty((n, n), dtype=torch.float32, device=dev)
+        mom_var = torch.empty((n, n), dtype=torch.float32, device=dev)
+        ws_m = ssb.Workspace(ssb.workspace_bytes(geom, n_bf, ssb.OP_MOMENTS), dev)
+        t_mom = timed(lambda: ssb.phase_moments(G, geom, bfd, ab, mean=mom_mean, var=mom_var, ws=ws_m,
+                                                stream=stream), reps=5)
+        gb = entries * 8
+        compact["phase_moments"] = {"ms": t_mom, "G_GBs": gb / (t_mom * 1e-3) / 1e9,
+                                    "G_hbm_frac": gb / (t_mom * 1e-3) / 1e9 / hbm,
+                                    "atan2_per_s": n_bf * n * n / (t_mom * 1e-3),
+                                    "planes_per_s": n_bf / (t_mom * 1e-3)}
+        del ws_m
         torch.cuda.synchronize()
 
     stage_rooflines = {

@@ -26,7 +26,7 @@ LIB_PATH = os.path.join(_HERE, "libssb.so")
 
 SSB_OK, SSB_INVALID_ARG, SSB_UNSUPPORTED, SSB_WORKSPACE_TOO_SMALL, SSB_CUDA_ERROR = range(5)
 SSB_U16, SSB_F32 = 0, 1
-OP_BUILD, OP_RECON, OP_SCORE = 0, 1, 2
+OP_BUILD, OP_RECON, OP_SCORE, OP_MOMENTS = 0, 1, 2, 3
 MAX_SETS = 8
 
 STATUS_NAMES = {0: "SSB_OK", 1: "SSB_INVALID_ARG", 2: "SSB_UNSUPPORTED",
@@ -35,7 +35,8 @@ STATUS_NAMES = {0: "SSB_OK", 1: "SSB_INVALID_ARG", 2: "SSB_UNSUPPORTED",
 EXPORTED = ("ssb_bf_indices", "ssb_band_indices", "ssb_workspace_bytes", "ssb_build_G",
             "ssb_reconstruct", "ssb_score_batch", "ssb_last_error", "ssb_launch_count",
             "ssb_reconstruct_noalloc", "ssb_build_G_host", "ssb_build_G_host_bytes",
-            "ssb_compact_G16", "ssb_compact_band", "ssb_reconstruct_g", "ssb_score_batch_g")
+            "ssb_compact_G16", "ssb_compact_band", "ssb_reconstruct_g", "ssb_score_batch_g",
+            "ssb_phase_moments")
 
 G_C64, G_SN16 = 0, 1
 
@@ -119,11 +120,12 @@ def load(path: str | None = None):
     lib.ssb_reconstruct_g.argtypes = [S_p, G_p, c_vp, c_int, A_p, c_vp, c_vp, c_vp, c_vp, c_size, c_vp]
     lib.ssb_score_batch_g.argtypes = [S_p, G_p, c_vp, c_int, A_p, c_int, c_vp, c_int, c_vp, c_vp, c_vp,
                                       c_vp, c_size, c_vp]
+    lib.ssb_phase_moments.argtypes = [S_p, G_p, c_vp, c_int, A_p, c_vp, c_vp, c_vp, c_size, c_vp]
     lib.ssb_last_error.restype = ctypes.c_char_p
     lib.ssb_launch_count.restype = ctypes.c_longlong
     for fn in ("ssb_bf_indices", "ssb_band_indices", "ssb_build_G", "ssb_build_G_host", "ssb_reconstruct",
                "ssb_score_batch", "ssb_reconstruct_noalloc", "ssb_compact_G16", "ssb_compact_band",
-               "ssb_reconstruct_g", "ssb_score_batch_g"):
+               "ssb_reconstruct_g", "ssb_score_batch_g", "ssb_phase_moments"):
         getattr(lib, fn).restype = c_int
     _lib = lib
     return lib
@@ -429,3 +431,25 @@ def score_batch_g(store, geom, bf_idx_dev, sets, band_dev, O=None, N=None, score
                                                       arr, B, _ptr(band_dev), nq, _ptr(O), _ptr(N), _ptr(score),
                                                       ws.ptr(), ws.nbytes, _stream(stream)))
     return O, N, score
+
+
+def phase_moments(store, geom, bf_idx_dev, aberr, mean=None, var=None, ws=None, stream=None):
+    """Per-BF phase moments: (mean, var) float32 [n, n] over BF pixels of
+    atan2(b_k, a_k); store: a GStore or a complex64 half-plane G."""
+    import torch
+    lib = load()
+    if not isinstance(store, GStore):
+        store = GStore(store)
+    g = to_geometry(geom)
+    a = to_aberr(aberr)
+    n_bf = int(bf_idx_dev.numel())
+    dev = store.G.device
+    mean = torch.empty((g.n, g.n), dtype=torch.float32, device=dev) if mean is None else mean
+    var = torch.empty((g.n, g.n), dtype=torch.float32, device=dev) if var is None else var
+    if ws is None:
+        ws = Workspace(workspace_bytes(g, n_bf, OP_MOMENTS), dev)
+    sc = store.c()
+    _check("ssb_phase_moments", lib.ssb_phase_moments(ctypes.byref(sc), ctypes.byref(g), _ptr(bf_idx_dev), n_bf,
+                                                      ctypes.byref(a), _ptr(mean), _ptr(var), ws.ptr(), ws.nbytes,
+                                                      _stream(stream)))
+    return mean, var

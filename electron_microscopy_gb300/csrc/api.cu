@@ -144,6 +144,18 @@ static WsLayout layout(const ssb_geometry* g, int n_bf, int op, int B, int nq) {
         L.total = off;
         return L;
     }
+    if (op == SSB_OP_MOMENTS) {
+        L.ktab = off;
+        off += align256((size_t)n_bf * sizeof(float4));
+        L.chik = off;
+        off += align256((size_t)n_bf * kChiStride * sizeof(float));
+        L.Y = off;
+        off += align256(moments_chunk_bytes(n));
+        L.Opart = off;  // the moment partial sums
+        off += align256(moments_part_bytes(n));
+        L.total = off;
+        return L;
+    }
     if (op == SSB_OP_RECON) {
         B = 1;
         nq = n * H;
@@ -295,7 +307,7 @@ size_t ssb_workspace_bytes(const ssb_geometry* geom, int n_bf, int op, int B, in
     if (check_geom(geom) != SSB_OK) return 0;
     if (n_bf < 1) return 0;
     if (op == SSB_OP_SCORE && (B < 1 || B > SSB_MAX_SETS || nq < 1)) return 0;
-    if (op != SSB_OP_BUILD && op != SSB_OP_RECON && op != SSB_OP_SCORE) return 0;
+    if (op != SSB_OP_BUILD && op != SSB_OP_RECON && op != SSB_OP_SCORE && op != SSB_OP_MOMENTS) return 0;
     return layout(geom, n_bf, op, B, nq).total;
 }
 
@@ -511,6 +523,40 @@ int ssb_score_batch_g(const ssb_gstore* G, const ssb_geometry* geom, const int32
                       int32_t* N_dev, double* score_dev, void* ws, size_t ws_bytes, void* stream) {
     return score_impl(G, geom, bf_idx_dev, n_bf, sets, B, band_dev, nq, O_dev, N_dev, score_dev, ws, ws_bytes,
                       stream);
+}
+
+int ssb_phase_moments(const ssb_gstore* store, const ssb_geometry* geom, const int32_t* bf_idx_dev, int n_bf,
+                      const ssb_aberr* set, float* mean_dev, float* var_dev, void* ws, size_t ws_bytes,
+                      void* stream) {
+    int rc;
+    if ((rc = check_geom(geom)) != SSB_OK) return rc;
+    GView gv{};
+    if ((rc = gview_of(store, geom, 0, &gv)) != SSB_OK) return rc;
+    if (gv.band) return fail(SSB_INVALID_ARG, "the phase moments need the half plane, not a band-compacted G");
+    if (!bf_idx_dev || !set || !mean_dev || !var_dev)
+        return fail(SSB_INVALID_ARG, "G, bf_idx, set, mean and var must not be NULL");
+    if (n_bf < 1 || (long long)n_bf > (long long)geom->det_y * geom->det_x)
+        return fail(SSB_INVALID_ARG, "n_bf=%d out of range", n_bf);
+    if ((rc = check_set(set)) != SSB_OK) return rc;
+    const WsLayout Lw = layout(geom, n_bf, SSB_OP_MOMENTS, 1, 0);
+    if ((rc = check_ws(ws, ws_bytes, Lw.total)) != SSB_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    SetBatch sb{};
+    sb.B = 1;
+    sb.r2 = aperture_r2(geom);
+    sb.s[0] = set_params(geom, set);
+    float2* tw = at<float2>(ws, Lw.tw);
+    float4* ktab = at<float4>(ws, Lw.ktab);
+    cudaError_t e;
+    if ((e = launch_twiddles(tw, geom->n, st)) != cudaSuccess) return cuda_fail(e, "twiddles");
+    if ((e = launch_prep(bf_idx_dev, n_bf, geom->det_x, geom->det_center_y, geom->det_center_x, geom->det_pitch_invA,
+                         sb, ktab, at<float>(ws, Lw.chik), gv, nullptr, st)) != cudaSuccess)
+        return cuda_fail(e, "prep");
+    if ((e = launch_moments(gv, geom->n, n_bf, ktab, sb, 1.0 / ((double)geom->n * geom->scan_step_A), tw,
+                            at<void>(ws, Lw.Y), at<void>(ws, Lw.Opart), mean_dev, var_dev, st)) != cudaSuccess)
+        return cuda_fail(e, "moments");
+    g_err[0] = 0;
+    return SSB_OK;
 }
 
 int ssb_compact_G16(const void* G_dev, const ssb_geometry* geom, int n_bf, int rows_per_scale, void* G16_dev,

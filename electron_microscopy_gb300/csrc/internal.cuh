@@ -326,6 +326,25 @@ __device__ __forceinline__ bool aperture_f32(float px, float py, float tx, float
     return d2 <= r2;
 }
 
+// w(q,k) G(q,k) added to acc: d = chi(k) - chi(k -/+ q) in turns, reduced to
+// [-1/2, 1/2] exactly.  T-: w = exp(-2 pi i d); T+: w = -exp(+2 pi i d), which
+// is the T- form with G and the angle negated: the caller passes
+// gs = +/-G and tw = +/-2 pi once per (q, k), and every set adds
+// gs exp(-i tw r) with four FMAs.
+__device__ __forceinline__ void accumulate(float2& acc, float2 gs, float chik, float chiq, float tw) {
+    const float d = __fsub_rn(chik, chiq);
+    const float r = __fsub_rn(d, rintf(d));
+    float sn, cs;
+    __sincosf(__fmul_rn(tw, r), &sn, &cs);  // |argument| <= pi
+    acc.x = __fmaf_rn(gs.y, sn, __fmaf_rn(gs.x, cs, acc.x));
+    acc.y = __fmaf_rn(-gs.x, sn, __fmaf_rn(gs.y, cs, acc.y));
+}
+
+__device__ __forceinline__ float2 side_sign(float2 g, bool minus) {
+    return minus ? g : make_float2(-g.x, -g.y);
+}
+constexpr float kTwoPi = 6.28318530717958648f;
+
 // ---------------------------------------------------------------------------
 // host-side launchers (defined in build.cu / reduce.cu); return cudaError_t
 // ---------------------------------------------------------------------------
@@ -397,6 +416,12 @@ cudaError_t launch_phase(const float2* O, const int32_t* N, const double* dcpart
                          cudaStream_t st);
 cudaError_t launch_score(const float2* O, const int32_t* N, int B, int nq, double* score,
                          cudaStream_t st);
+// per-BF phase moments (moments.cu): Y holds moments_chunk_bytes(n), part
+// moments_part_bytes(n)
+size_t moments_chunk_bytes(int n);
+size_t moments_part_bytes(int n);
+cudaError_t launch_moments(const GView& g, int n, int n_bf, const float4* ktab, const SetBatch& sb, double dq,
+                           const float2* tw, void* Y, void* part, float* mean, float* var, cudaStream_t st);
 // compact storage (compact.cu)
 cudaError_t launch_compact_g16(const float2* G, int n, int n_bf, int srows, uint32_t* G16, float* scale,
                                cudaStream_t st);

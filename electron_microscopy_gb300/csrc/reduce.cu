@@ -93,25 +93,6 @@ constexpr int kKChunk = 64;  // k pixels whose tables a block stages at a time
 template <int MAXB>
 __host__ __device__ constexpr int red_unroll() { return MAXB == 1 ? 8 : 4; }
 
-// w(q,k) G(q,k) added to acc: d = chi(k) - chi(k -/+ q) in turns, reduced to
-// [-1/2, 1/2] exactly.  T-: w = exp(-2 pi i d); T+: w = -exp(+2 pi i d), which
-// is the T- form with G and the angle negated: the caller passes
-// gs = +/-G and tw = +/-2 pi once per (q, k), and every set adds
-// gs exp(-i tw r) with four FMAs.
-__device__ __forceinline__ void accumulate(float2& acc, float2 gs, float chik, float chiq, float tw) {
-    const float d = __fsub_rn(chik, chiq);
-    const float r = __fsub_rn(d, rintf(d));
-    float sn, cs;
-    __sincosf(__fmul_rn(tw, r), &sn, &cs);  // |argument| <= pi
-    acc.x = __fmaf_rn(gs.y, sn, __fmaf_rn(gs.x, cs, acc.x));
-    acc.y = __fmaf_rn(-gs.x, sn, __fmaf_rn(gs.y, cs, acc.y));
-}
-
-__device__ __forceinline__ float2 side_sign(float2 g, bool minus) {
-    return minus ? g : make_float2(-g.x, -g.y);
-}
-constexpr float kTwoPi = 6.28318530717958648f;
-
 // Row tables of the batched forms: per warp, up to kRowSlots distinct scan
 // rows (q_y) among its 32 lanes (neighbouring entries: normally 1 or 2), per
 // trotter side and set one float4 (a3, a2, a1, a0); the set index is padded

@@ -100,7 +100,7 @@ typedef enum ssb_status {
     SSB_CUDA_ERROR = 4            /* a launch failed; see ssb_last_error()             */
 } ssb_status;
 
-typedef enum ssb_op { SSB_OP_BUILD = 0, SSB_OP_RECON = 1, SSB_OP_SCORE = 2 } ssb_op;
+typedef enum ssb_op { SSB_OP_BUILD = 0, SSB_OP_RECON = 1, SSB_OP_SCORE = 2, SSB_OP_MOMENTS = 3 } ssb_op;
 
 #define SSB_MAX_SETS 8
 #define SSB_MIN_N 8
@@ -130,8 +130,9 @@ int ssb_band_indices(const ssb_geometry* geom, double qmin, double qmax,
 
 /*
  * Bytes of device workspace an operation needs (0 on invalid arguments).
- * op = SSB_OP_BUILD, SSB_OP_RECON (B ignored, nq ignored) or SSB_OP_SCORE
- * (B sets over nq band entries).  The workspace must be 256-byte aligned.
+ * op = SSB_OP_BUILD, SSB_OP_RECON (B ignored, nq ignored), SSB_OP_SCORE
+ * (B sets over nq band entries) or SSB_OP_MOMENTS (B, nq ignored).  The
+ * workspace must be 256-byte aligned.
  */
 size_t ssb_workspace_bytes(const ssb_geometry* geom, int n_bf, int op, int B, int nq);
 
@@ -287,6 +288,26 @@ int ssb_score_batch_g(const ssb_gstore* G, const ssb_geometry* geom,
                       const int32_t* bf_idx_dev, int n_bf, const ssb_aberr* sets, int B,
                       const int32_t* band_dev, int nq,
                       void* O_dev, int32_t* N_dev, double* score_dev,
+                      void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Per-BF phase moments at one aberration set (set: host pointer): for every BF
+ * pixel k, the corrected plane S_k(q) = G(q,k) w(q,k) on the trotter pixels
+ * of k (0 elsewhere, and at DC and on the Nyquist row and column), its image
+ * b_k = irfft2(-i S_k) (numpy semantics) and the angle atan2(b_k, a_k) with
+ * a_k = Re G(0,k) / n^2; writes the mean over the n_bf pixels (mean_dev) and
+ * the population variance (var_dev), float32 [n][n] each, row = scan_y.  The
+ * sums are deterministic (fixed order; float32 within groups of at most 4 BF
+ * pixels, float64 across them).  G: host pointer to the descriptor; the half
+ * plane is needed (G->band_compact must be 0).  Source: "Historical WebGPU
+ * G(q,k) memory experiment", section "Object-redraw fast path" (the exact
+ * per-BF path, mean(angle(object)), and the variance the loss uses);
+ * "Tilt-corrected SSB on CUDA", sections "Changes" (Loss path) and "Open".
+ * Errors as ssb_reconstruct_g.
+ */
+int ssb_phase_moments(const ssb_gstore* G, const ssb_geometry* geom,
+                      const int32_t* bf_idx_dev, int n_bf, const ssb_aberr* set,
+                      float* mean_dev, float* var_dev,
                       void* ws, size_t ws_bytes, void* stream);
 
 /*

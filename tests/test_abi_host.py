@@ -88,6 +88,10 @@ def test_workspace_bytes(lib):
     assert ssb.workspace_bytes(g, 9354, ssb.OP_SCORE, 9, 44247) == 0
     assert ssb.workspace_bytes(g, 0, ssb.OP_RECON) == 0
     assert ssb.workspace_bytes(g, 10, 7) == 0
+    m = ssb.workspace_bytes(g, 9354, ssb.OP_MOMENTS)
+    # one chunk of 32 corrected half planes plus 8 float64 (sum, square) images
+    assert m >= 32 * 512 * 257 * 8 + 8 * 512 * 512 * 16
+    assert ssb.workspace_bytes(g, 0, ssb.OP_MOMENTS) == 0
     bad = C.Geometry(**{**g.__dict__, "n": 100})
     assert ssb.workspace_bytes(bad, 10, ssb.OP_RECON) == 0
 
@@ -247,4 +251,33 @@ def test_error_codes_compact_storage(lib):
     assert rc == ssb.SSB_INVALID_ARG
     assert lib.ssb_reconstruct_g(None, ctypes.byref(g), FAKE, 10, ctypes.byref(a), FAKE, FAKE, FAKE, FAKE, big,
                                  None) == ssb.SSB_INVALID_ARG
+    assert lib.ssb_launch_count() == before
+
+
+def test_error_codes_phase_moments(lib):
+    g = _g()
+    a = ssb.Aberr()
+    S = ssb.GStoreC
+    big = 1 << 30
+    before = lib.ssb_launch_count()
+    ok = S(FAKE.value, ssb.G_C64, 0, 0, 0)
+    banded = S(FAKE.value, ssb.G_C64, 0, 0, 1)
+    nan = ssb.Aberr(C30=float("inf"))
+    cases = [
+        ((None, ctypes.byref(g), FAKE, 10, ctypes.byref(a), FAKE, FAKE, FAKE, big, None), ssb.SSB_INVALID_ARG),
+        ((ctypes.byref(banded), ctypes.byref(g), FAKE, 10, ctypes.byref(a), FAKE, FAKE, FAKE, big, None),
+         ssb.SSB_INVALID_ARG),
+        ((ctypes.byref(ok), ctypes.byref(g), FAKE, 10, ctypes.byref(a), None, FAKE, FAKE, big, None),
+         ssb.SSB_INVALID_ARG),
+        ((ctypes.byref(ok), ctypes.byref(g), FAKE, 0, ctypes.byref(a), FAKE, FAKE, FAKE, big, None),
+         ssb.SSB_INVALID_ARG),
+        ((ctypes.byref(ok), ctypes.byref(g), FAKE, 10, ctypes.byref(nan), FAKE, FAKE, FAKE, big, None),
+         ssb.SSB_INVALID_ARG),
+        ((ctypes.byref(ok), ctypes.byref(g), FAKE, 10, ctypes.byref(a), FAKE, FAKE, FAKE, 1000, None),
+         ssb.SSB_WORKSPACE_TOO_SMALL),
+        ((ctypes.byref(ok), ctypes.byref(_g(n=12)), FAKE, 10, ctypes.byref(a), FAKE, FAKE, FAKE, big, None),
+         ssb.SSB_UNSUPPORTED),
+    ]
+    for args, code in cases:
+        assert lib.ssb_phase_moments(*args) == code, _err(lib)
     assert lib.ssb_launch_count() == before

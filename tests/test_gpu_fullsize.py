@@ -148,3 +148,59 @@ def test_batched_scores_sampled(full):
     for s in range(8):
         ref = np.sum(np.abs(Oh[s]) ** 2) / np.sum(Nh[s])
         assert abs(sc[s].item() - ref) <= 1e-9 * ref
+
+
+def test_phase_moments_sampled_pixels(full):
+    """The per-BF moments path at full size on three BF pixels the oracle
+    rebuilds from their traces: mean and variance over those pixels."""
+    ssb, geom, ab = full["ssb"], full["geom"], full["ab"]
+    n = geom.n
+    nbf = len(full["bf"])
+    idx = np.array([0, nbf // 2, nbf - 1])
+    sel = torch.from_numpy(idx).cuda()
+    mean, var = ssb.phase_moments(full["G"].index_select(0, sel).contiguous(), geom,
+                                  full["bfd"].index_select(0, sel).contiguous(), ab)
+    torch.cuda.synchronize()
+    Gor = np.stack([np.fft.rfft2(full["cols"][:, b].astype(np.float64).reshape(n, n)) for b in idx])
+    mref, vref = O.phase_moments(Gor, geom, ab, full["bf"][idx])
+    assert rel(mean.cpu().numpy(), mref) < TOL
+    assert rel(var.cpu().numpy(), vref) < TOL
+
+
+def test_phase_moments_all_pixels(full):
+    """Every BF pixel, as the bench runs it: finite, non-negative variance,
+    and the mean of angles tracks the angle of the mean object (the single
+    image)."""
+    ssb = full["ssb"]
+    mean, var = ssb.phase_moments(full["G"], full["geom"], full["bfd"], full["ab"])
+    torch.cuda.synchronize()
+    m = mean.cpu().numpy()
+    assert np.all(np.isfinite(m)) and var.min().item() >= 0
+    r = np.corrcoef(m.ravel(), full["phase"].cpu().numpy().ravel())[0, 1]
+    assert r > 0.5
+
+
+def test_compact_storage_full(full):
+    """herm16 (one scale per q row) and the band copy at full size: the
+    encoding bound on sampled planes, the band copy equal to the gather of
+    its source, and the reconstruction from herm16 close to the exact one."""
+    ssb, geom, ab = full["ssb"], full["geom"], full["ab"]
+    G = full["G"]
+    st = ssb.compact_G16(G, geom, 1)
+    band = ssb.band_indices(geom, *C.BAND_INVA)
+    bd = torch.from_numpy(band).cuda()
+    Gb = ssb.compact_band(st, geom, bd)
+    torch.cuda.synchronize()
+    sc = st.scale.cpu().numpy()
+    for b in (0, 4321, G.shape[0] - 1):
+        g = G[b].cpu().numpy()
+        c = st.G[b].cpu().numpy().view(np.int16).reshape(g.shape + (2,)).astype(np.float64)
+        s = sc[:, b].astype(np.float64)[:, None]
+        bound = s * ((0.5 + 2.0 ** -10) / 32767 + 2.0 ** -22)
+        assert np.all(np.abs(np.maximum(c[..., 0] / 32767, -1) * s - g.real) <= bound)
+        assert np.all(np.abs(np.maximum(c[..., 1] / 32767, -1) * s - g.imag) <= bound)
+        assert np.array_equal(Gb.G[b].cpu().numpy(), st.G[b].cpu().numpy().ravel()[band])
+    _, _, ph16 = ssb.reconstruct_g(st, geom, full["bfd"], ab)
+    ph = full["phase"].cpu().numpy()
+    span = float(ph.max() - ph.min())
+    assert np.abs(ph16.cpu().numpy() - ph).max() < 1e-3 * span
