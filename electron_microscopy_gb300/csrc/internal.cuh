@@ -180,7 +180,13 @@ template <> struct Dft<32> {
 // NS: span of the sub-transforms already done; TWS: stride into the
 // length-n twiddle table (n / L).
 // ---------------------------------------------------------------------------
-template <int L, int R, int NS, int TWS>
+// SWZ: the buffer holds point i at swz(i) = i ^ ((i >> 4) & 15), a bijection
+// within each 16-point block that makes both the stride-R writes of a pass
+// and the unit-stride reads of the next hit every bank pair at most twice
+// per warp (8-byte points)
+__device__ __forceinline__ int swz(int i) { return i ^ ((i >> 4) & 15); }
+
+template <int L, int R, int NS, int TWS, bool SWZ = false>
 __device__ __forceinline__ void stockham_pass(float2* buf, const float2* tw, int lane) {
     constexpr int NB = L / R;
     constexpr int PER = (NB + 31) / 32;
@@ -190,7 +196,7 @@ __device__ __forceinline__ void stockham_pass(float2* buf, const float2* tw, int
         const int j = lane + 32 * t;
         if (NB >= 32 || j < NB) {
 #pragma unroll
-            for (int r = 0; r < R; ++r) v[t][r] = buf[j + r * NB];
+            for (int r = 0; r < R; ++r) v[t][r] = buf[SWZ ? swz(j + r * NB) : j + r * NB];
         }
     }
     __syncwarp();
@@ -207,26 +213,27 @@ __device__ __forceinline__ void stockham_pass(float2* buf, const float2* tw, int
             Dft<R>::run(v[t]);
             const int base = (j - k) * R + k;
 #pragma unroll
-            for (int r = 0; r < R; ++r) buf[base + r * NS] = v[t][r];
+            for (int r = 0; r < R; ++r) buf[SWZ ? swz(base + r * NS) : base + r * NS] = v[t][r];
         }
     }
     __syncwarp();
 }
 
-template <int L, int NS, int TWS>
+template <int L, int NS, int TWS, bool SWZ>
 __device__ __forceinline__ void fft_passes(float2* buf, const float2* tw, int lane) {
     if constexpr (NS < L) {
         constexpr int REM = L / NS;
         constexpr int R = (REM >= 8) ? 8 : REM;
-        stockham_pass<L, R, NS, TWS>(buf, tw, lane);
-        fft_passes<L, NS * R, TWS>(buf, tw, lane);
+        stockham_pass<L, R, NS, TWS, SWZ>(buf, tw, lane);
+        fft_passes<L, NS * R, TWS, SWZ>(buf, tw, lane);
     }
 }
 
 // Forward complex FFT (exp(-2 pi i ...)) of length L, in place, by one warp.
-template <int L, int TWS>
+// SWZ: input and output are in the swizzled order swz(i) (see stockham_pass).
+template <int L, int TWS, bool SWZ = false>
 __device__ __forceinline__ void fft_warp(float2* buf, const float2* tw, int lane) {
-    fft_passes<L, 1, TWS>(buf, tw, lane);
+    fft_passes<L, 1, TWS, SWZ>(buf, tw, lane);
 }
 
 // ---------------------------------------------------------------------------

@@ -30,14 +30,19 @@ namespace ssb {
 
 constexpr int kMomThreads = 256;
 
-// one k of a stored G at half-plane entry e of row `row` (herm16: dequantised)
+// one k of a stored G at half-plane entry e of row `row` (herm16: dequantised);
+// STREAM: read once, evict first, so G passing through does not push the
+// chunk and the partial sums out of L2
+template <bool STREAM = false>
 __device__ __forceinline__ float2 g_entry(const GView& g, int n_bf, int k, size_t e, int row) {
     if (g.fmt == kGSN16) {
-        const uint32_t w = static_cast<const uint32_t*>(g.G)[(size_t)k * g.stride + e];
+        const uint32_t* p = static_cast<const uint32_t*>(g.G) + (size_t)k * g.stride + e;
+        const uint32_t w = STREAM ? __ldcs(p) : *p;
         const float s = g.scale[(size_t)(g.srows == 1 ? row : 0) * n_bf + k];
         return sn16_unpack(w, __fmul_rn(s, kInv32767));
     }
-    return static_cast<const float2*>(g.G)[(size_t)k * g.stride + e];
+    const float2* p = static_cast<const float2*>(g.G) + (size_t)k * g.stride + e;
+    return STREAM ? __ldcs(p) : *p;
 }
 
 // 1. Y[kk][e] = -i S_{k0+kk}(q_e): thread e of block row y walks BF pixels
@@ -64,7 +69,7 @@ ssb_correct(GView g, int n_bf, const float4* __restrict__ ktab, SetBatch sb, int
 #pragma unroll
         for (int u = 0; u < kMomUnroll; ++u) {
             const int kk = kb + u * kMomKSplit;
-            gv[u] = kk < kc ? g_entry(g, n_bf, k0 + kk, (size_t)e, row) : make_float2(0.f, 0.f);
+            gv[u] = kk < kc ? g_entry<true>(g, n_bf, k0 + kk, (size_t)e, row) : make_float2(0.f, 0.f);
         }
 #pragma unroll
         for (int u = 0; u < kMomUnroll; ++u) {
@@ -101,7 +106,9 @@ ssb_inv_cols(float2* __restrict__ Y, const float2* __restrict__ twg, int items) 
     constexpr int H = N / 2 + 1;
     constexpr int CW = inv_cols_width<N>();
     constexpr int NG = (N / 2) / CW;
-    constexpr int CS = N + 1;
+    // column stride N + 4 and rows stored swizzled: the transposes and the
+    // FFT passes hit each bank pair at most twice per warp
+    constexpr int CS = N + 4;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     float2* tw = reinterpret_cast<float2*>(smem_raw);
     float2* cols = tw + N;
@@ -116,30 +123,46 @@ ssb_inv_cols(float2* __restrict__ Y, const float2* __restrict__ twg, int items) 
         const int nc = CW + ((grp == NG - 1) ? 1 : 0);
         // CW columns per group (compile-time index split), plus column N/2
         // in the last group; inverse via conj(FFT(conj(.)))
-        for (int idx = threadIdx.x; idx < N * CW; idx += kMomThreads) {
-            const int row = idx / CW, c = idx % CW;
-            cols[c * CS + row] = cconj(y[(size_t)row * H + c0 + c]);
+        if constexpr ((N * CW) % kMomThreads == 0) {
+            // every load of the item in flight at once, then into shared memory
+            constexpr int LPT = N * CW / kMomThreads;
+            float2 v[LPT];
+#pragma unroll
+            for (int i = 0; i < LPT; ++i) {
+                const int idx = threadIdx.x + i * kMomThreads;
+                v[i] = y[(size_t)(idx / CW) * H + c0 + idx % CW];
+            }
+#pragma unroll
+            for (int i = 0; i < LPT; ++i) {
+                const int idx = threadIdx.x + i * kMomThreads;
+                cols[(idx % CW) * CS + swz(idx / CW)] = cconj(v[i]);
+            }
+        } else {
+            for (int idx = threadIdx.x; idx < N * CW; idx += kMomThreads) {
+                const int row = idx / CW, c = idx % CW;
+                cols[c * CS + swz(row)] = cconj(y[(size_t)row * H + c0 + c]);
+            }
         }
         if (nc > CW)
             for (int row = threadIdx.x; row < N; row += kMomThreads)
-                cols[CW * CS + row] = cconj(y[(size_t)row * H + N / 2]);
+                cols[CW * CS + swz(row)] = cconj(y[(size_t)row * H + N / 2]);
         __syncthreads();
-        for (int c = warp; c < nc; c += NW) fft_warp<N, 1>(cols + c * CS, tw, lane);
+        for (int c = warp; c < nc; c += NW) fft_warp<N, 1, true>(cols + c * CS, tw, lane);
         __syncthreads();
         for (int idx = threadIdx.x; idx < N * CW; idx += kMomThreads) {
             const int row = idx / CW, c = idx % CW;
-            y[(size_t)row * H + c0 + c] = cconj(cols[c * CS + row]);
+            y[(size_t)row * H + c0 + c] = cconj(cols[c * CS + swz(row)]);
         }
         if (nc > CW)
             for (int row = threadIdx.x; row < N; row += kMomThreads)
-                y[(size_t)row * H + N / 2] = cconj(cols[CW * CS + row]);
+                y[(size_t)row * H + N / 2] = cconj(cols[CW * CS + swz(row)]);
     }
 }
 
 // 3. C2R along q_x (numpy irfft semantics), atan2, moment sums: block
 // (8 rows, plane group p) walks planes [p * per, (p + 1) * per) of the chunk
-constexpr int kMomGroups = 16;
-constexpr int kMomChunk = 64;
+constexpr int kMomGroups = 8;   // 8 float64 (sum, square) images: 33.5 MB at n = 512
+constexpr int kMomChunk = 64;   // 64 corrected half planes: 67 MB; both stay in L2
 
 template <int N>
 __global__ void __launch_bounds__(kMomThreads)
@@ -181,23 +204,23 @@ ssb_inv_rows_moments(const float2* __restrict__ Y, int kc, GView g, int n_bf, in
             const float2 xc = cconj(xl);
             const float2 ev = cadd(xk, xc);
             const float2 od = cmul(csub(xk, xc), cconj(tw[k]));
-            z[k] = cconj(cadd(ev, cmul_pi(od)));  // inverse via conj trick
+            z[swz(k)] = cconj(cadd(ev, cmul_pi(od)));  // inverse via conj trick
         }
         __syncwarp();
-        fft_warp<L, 2>(z, tw, lane);
+        fft_warp<L, 2, true>(z, tw, lane);
 #pragma unroll
         for (int j = 0; j < PER; ++j) {
             const int m = lane + 32 * j;
             if (m < L) {
-                const float2 v = cconj(z[m]);
+                const float2 v = cconj(z[swz(m)]);
                 const float t0 = atan2f(v.x * inv, a), t1 = atan2f(v.y * inv, a);
-                float2 u0 = s12[2 * m], u1 = s12[2 * m + 1];
-                u0.x += t0;
-                u0.y = __fmaf_rn(t0, t0, u0.y);
-                u1.x += t1;
-                u1.y = __fmaf_rn(t1, t1, u1.y);
-                s12[2 * m] = u0;
-                s12[2 * m + 1] = u1;
+                // (sum, square) of outputs 2m and 2m + 1 as one 16-byte access
+                float4 u = reinterpret_cast<float4*>(s12)[m];
+                u.x += t0;
+                u.y = __fmaf_rn(t0, t0, u.y);
+                u.z += t1;
+                u.w = __fmaf_rn(t1, t1, u.w);
+                reinterpret_cast<float4*>(s12)[m] = u;
             }
         }
         __syncwarp();
@@ -235,7 +258,7 @@ static cudaError_t moments_n(const GView& g, int n_bf, const float4* ktab, const
     constexpr int CW = inv_cols_width<N>();
     constexpr int NG = (N / 2) / CW;
     constexpr int RPB = kMomThreads / 32;
-    const size_t cs = (size_t)N * sizeof(float2) + (size_t)(CW + 1) * (N + 1) * sizeof(float2);
+    const size_t cs = (size_t)N * sizeof(float2) + (size_t)(CW + 1) * (N + 4) * sizeof(float2);
     const size_t rs = (size_t)N * sizeof(float2) + (size_t)RPB * (N / 2) * sizeof(float2) +
                       (size_t)RPB * N * sizeof(float2);
     cudaError_t e;
