@@ -6,8 +6,12 @@ exchange, and the reduction shards over k with one all-reduce (sum) of O, N
 and the G(0,k) sum, after which any rank forms the image ("Tilt-corrected
 SSB on CUDA", Where the time went: the reduction is a sum over BF pixels per
 frequency; "Historical WebGPU G(q,k) memory experiment", Implementation: G is
-built per BF pixel).  These tests run that plan on two gloo ranks with the
-oracle as the per-rank compute and compare it with the single-process oracle.
+built per BF pixel).  The per-BF phase moments shard the same way: each rank sums the angles of its
+own BF pixels' images and their squares, and one all-reduce of those two
+images gives the mean and variance over all pixels ("Historical WebGPU G(q,k)
+memory experiment", Object-redraw fast path: the exact path is a mean over BF
+pixels).  These tests run that plan on two gloo ranks with the oracle as the
+per-rank compute and compare it with the single-process oracle.
 """
 import os
 import socket
@@ -51,6 +55,13 @@ def _rank_main(rank, world, port, out_dir, name):
         for o, nn in Ob:
             parts.append(torch.from_numpy(np.ascontiguousarray(o).view(np.float64).copy()))
             parts.append(torch.from_numpy(nn.astype(np.int64)))
+        n = g.n
+        s1, s2 = np.zeros((n, n)), np.zeros((n, n))
+        for a, b in O.per_bf_images(G, g, ab, mine):    # this rank's BF pixels only
+            t = np.arctan2(b, a)
+            s1 += t
+            s2 += t * t
+        parts += [torch.from_numpy(s1), torch.from_numpy(s2)]
         for t in parts:
             dist.all_reduce(t, op=dist.ReduceOp.SUM)
         if rank == 0:
@@ -97,3 +108,10 @@ def test_k_sharded_reduction_matches_single_process(name):
         np.testing.assert_array_equal(n_sh, n_ref)
         assert np.linalg.norm(o_sh - o_ref) <= 1e-12 * max(np.linalg.norm(o_ref), 1e-300)
         assert abs(O.score(o_sh, n_sh) - O.score(o_ref, n_ref)) <= 1e-12 * max(O.score(o_ref, n_ref), 1e-300)
+
+    # per-BF moments from the all-reduced angle sums
+    mean_ref, var_ref = O.phase_moments(ref["G"], g, ab, bf)
+    mean_sh = parts[7] / len(bf)
+    var_sh = np.maximum(parts[8] / len(bf) - mean_sh * mean_sh, 0.0)
+    np.testing.assert_allclose(mean_sh, mean_ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(var_sh, var_ref, rtol=0, atol=1e-12)
