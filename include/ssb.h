@@ -257,7 +257,8 @@ int ssb_compact_G16(const void* G_dev, const ssb_geometry* geom, int n_bf, int r
  * Band-compacted copy of a half-plane G (src->band_compact must be 0; only
  * src->G and src->fmt are read): dst_dev[k][i] = G[k][band[i]], 8-byte entries
  * for SSB_G_C64, 4-byte words for SSB_G_SN16.  band_dev: device int32[nq] of
- * half-plane entries (as ssb_band_indices writes them).  Bit-exact copy.
+ * half-plane entries (as ssb_band_indices writes them).  Bit-exact copy;
+ * dst_dev must not overlap the source.
  * Errors: SSB_INVALID_ARG for a null pointer, n_bf < 1, nq out of
  * [1, n*(n/2+1)], an unknown format or a band-compacted source.
  */
