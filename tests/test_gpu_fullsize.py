@@ -10,6 +10,10 @@ positions), N(q) at a few thousand q, and the batched scores' O/N over the
 band at sampled entries.  The phase image stage runs in the same launch
 geometry as the n = 512 case of test_gpu_parity (checked element by element
 there); here it is checked for finiteness and recovery of the ground truth.
+The compact forms and the per-BF moments run at full size too: the herm16
+encoding bound on sampled planes, the band copy against its source, the
+herm16 phase against the exact one, and the moments on three BF pixels the
+oracle rebuilds from their traces.
 """
 import numpy as np
 import pytest
