@@ -423,19 +423,48 @@ int ssb_build_G_host(const void* frames_host, int dtype, const ssb_geometry* geo
                        ws_bytes - H.build, stream);
 }
 
-static int reconstruct_impl(const ssb_gstore* store, const ssb_geometry* geom, const int32_t* bf_idx_dev, int n_bf,
-                            const ssb_aberr* set, void* O_dev, int32_t* N_dev, float* phase_dev, void* ws,
-                            size_t ws_bytes, void* stream) {
+static ssb_gstore c64_store(const void* G_dev) {
+    ssb_gstore s{};
+    s.G = G_dev;
+    s.fmt = SSB_G_C64;
+    return s;
+}
+
+// every argument check of a reconstruction except the workspace's
+static int check_recon_args(const ssb_gstore* store, const ssb_geometry* geom, const int32_t* bf_idx_dev, int n_bf,
+                            const ssb_aberr* set, const void* O_dev, const int32_t* N_dev, const float* phase_dev,
+                            GView* gv) {
     int rc;
     if ((rc = check_geom(geom)) != SSB_OK) return rc;
-    GView gv{};
-    if ((rc = gview_of(store, geom, 0, &gv)) != SSB_OK) return rc;
-    if (gv.band) return fail(SSB_INVALID_ARG, "a reconstruction needs the half plane, not a band-compacted G");
+    if ((rc = gview_of(store, geom, 0, gv)) != SSB_OK) return rc;
+    if (gv->band) return fail(SSB_INVALID_ARG, "a reconstruction needs the half plane, not a band-compacted G");
     if (!bf_idx_dev || !set || !O_dev || !N_dev || !phase_dev)
         return fail(SSB_INVALID_ARG, "G, bf_idx, set, O, N and phase must not be NULL");
     if (n_bf < 1 || (long long)n_bf > (long long)geom->det_y * geom->det_x)
         return fail(SSB_INVALID_ARG, "n_bf=%d out of range", n_bf);
-    if ((rc = check_set(set)) != SSB_OK) return rc;
+    return check_set(set);
+}
+
+}  // extern "C"
+
+namespace ssb {
+int check_reconstruct_args(const void* G_dev, const ssb_geometry* geom, const int32_t* bf_idx_dev, int n_bf,
+                           const ssb_aberr* set, const void* O_dev, const int32_t* N_dev, const float* phase_dev) {
+    const ssb_gstore s = c64_store(G_dev);
+    GView gv{};
+    return check_recon_args(&s, geom, bf_idx_dev, n_bf, set, O_dev, N_dev, phase_dev, &gv);
+}
+}  // namespace ssb
+
+extern "C" {
+
+static int reconstruct_impl(const ssb_gstore* store, const ssb_geometry* geom, const int32_t* bf_idx_dev, int n_bf,
+                            const ssb_aberr* set, void* O_dev, int32_t* N_dev, float* phase_dev, void* ws,
+                            size_t ws_bytes, void* stream) {
+    int rc;
+    GView gv{};
+    if ((rc = check_recon_args(store, geom, bf_idx_dev, n_bf, set, O_dev, N_dev, phase_dev, &gv)) != SSB_OK)
+        return rc;
     const WsLayout Lw = layout(geom, n_bf, SSB_OP_RECON, 1, 0);
     if ((rc = check_ws(ws, ws_bytes, Lw.total)) != SSB_OK) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -488,13 +517,6 @@ static int score_impl(const ssb_gstore* store, const ssb_geometry* geom, const i
         return cuda_fail(e, "score");
     g_err[0] = 0;
     return SSB_OK;
-}
-
-static ssb_gstore c64_store(const void* G_dev) {
-    ssb_gstore s{};
-    s.G = G_dev;
-    s.fmt = SSB_G_C64;
-    return s;
 }
 
 int ssb_reconstruct(const void* G_dev, const ssb_geometry* geom, const int32_t* bf_idx_dev, int n_bf,

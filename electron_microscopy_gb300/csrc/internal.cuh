@@ -435,6 +435,12 @@ cudaError_t launch_compact_g16(const float2* G, int n, int n_bf, int srows, uint
 cudaError_t launch_compact_band(const void* G, int fmt, size_t plane, int n_bf, const int32_t* band, int nq,
                                 void* dst, cudaStream_t st);
 
+// the argument checks of ssb_reconstruct on a complex64 G, without the
+// workspace's (api.cu): SSB_OK or the status ssb_reconstruct would return,
+// with the message set
+int check_reconstruct_args(const void* G_dev, const ssb_geometry* geom, const int32_t* bf_idx_dev, int n_bf,
+                           const ssb_aberr* set, const void* O_dev, const int32_t* N_dev, const float* phase_dev);
+
 // launch bookkeeping (api.cu)
 void count_launch(int k = 1);
 

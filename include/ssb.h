@@ -323,12 +323,16 @@ int ssb_phase_moments(const ssb_gstore* G, const ssb_geometry* geom,
  * fixed array of SSB_NOALLOC_SCRATCH_BYTES inside the library (held by every
  * GPU that loads the library until the process exits) instead of a caller
  * workspace.  It calls no allocating routine.
- *   - Calls whose scratch need, ssb_workspace_bytes(geom, n_bf, SSB_OP_RECON,
- *     1, 1), exceeds SSB_NOALLOC_SCRATCH_BYTES return SSB_UNSUPPORTED before
- *     launching anything (every n <= 512 fits; n = 1024 does not).
- *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current) and caches it; make that
- *     first call before any stream capture.
+ *   - The arguments are checked first, as ssb_reconstruct checks them (same
+ *     status codes).  Then calls whose scratch need,
+ *     ssb_workspace_bytes(geom, n_bf, SSB_OP_RECON, 1, 1), exceeds
+ *     SSB_NOALLOC_SCRATCH_BYTES return SSB_UNSUPPORTED before launching
+ *     anything (every n <= 512 fits; n = 1024 does not).
+ *   - Every call looks up the array's device address on the current device
+ *     (cudaGetSymbolAddress, a host-side lookup; nothing is cached, so calls
+ *     after a device reset use the new context's array).  The first call on a
+ *     device may load the library's device code there: make it before any
+ *     stream capture.
  *   - All calls share the one array, which keeps the last call's contents;
  *     nothing in it needs to start at zero.  Calls that overlap on the GPU
  *     (different streams or host threads) race on it: serialise them.

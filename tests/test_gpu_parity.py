@@ -272,3 +272,77 @@ def test_build_G_host_equals_device_build(ssb, case, tiny_dataset, small_dataset
     assert torch.equal(Gh, Gd)
     if case != "n512":
         assert rel(Gh.cpu().numpy(), O.build_G(frames, bf)) < TOL
+
+
+# ----------------------------------------------------------------------------
+# batched scoring with a different probe tilt per set: the reduction then
+# takes each set's own aperture tests (its aperture bit at k, its trotter
+# classes at k -/+ q) instead of sharing one set of tests across the batch
+# ----------------------------------------------------------------------------
+
+# tilt offsets (mrad) added to the base tilt, set by set; the fourth moves the
+# disk by several detector pixels on both workloads below
+TILT_STEPS_MRAD = [(0.0, 0.0), (1.5, -0.5), (-2.0, 1.0), (9.0, -6.0), (0.4, 2.5), (-3.5, -3.0),
+                   (2.0, 2.0), (-0.8, 0.3)]
+
+
+def _tilted_sets(base, B, seed):
+    sets = C.perturbed_sets(base, B, seed=seed)
+    return [s.replace(tilt_x_rad=base.tilt_x_rad + dx * 1e-3, tilt_y_rad=base.tilt_y_rad + dy * 1e-3)
+            for s, (dx, dy) in zip(sets, TILT_STEPS_MRAD)]
+
+
+def _per_set_tilt_case(case, small_dataset):
+    if case == "small":
+        d = small_dataset
+        return d["frames"], d["geom"], d["ab"]
+    rng = np.random.default_rng(31)
+    n, det = 512, 20
+    frames = rng.poisson(3.0, size=(n, n, det, det)).astype(np.uint16)
+    return frames, _geom(n, det, 0.2), AB
+
+
+@pytest.mark.parametrize("case", ["small", "n512"])
+@pytest.mark.parametrize("B", [3, 8])
+def test_score_batch_per_set_tilts_match_oracle(ssb, case, B, small_dataset):
+    """Sets with distinct tilts: N bit-exact, O within 1e-4 and the score within
+    1e-4, set by set, against the oracle's reduction."""
+    frames, g, base = _per_set_tilt_case(case, small_dataset)
+    bf = O.bf_indices(g, base.tilt_x_rad, base.tilt_y_rad)
+    sets = _tilted_sets(base, B, seed=40 + B)
+    # the sets really differ in tilt, by several pixels for one of them
+    shift = max(C.tilt_shift_px(g, s.replace(tilt_x_rad=s.tilt_x_rad - base.tilt_x_rad,
+                                             tilt_y_rad=s.tilt_y_rad - base.tilt_y_rad)) for s in sets)
+    assert len({(s.tilt_x_rad, s.tilt_y_rad) for s in sets}) == B and shift > 1.5
+    band = O.band_indices(g, 0.2, 0.9)
+    G = ssb.build_G(_frames_dev(frames), g, _dev(bf))
+    Ob, Nb, sc = ssb.score_batch(G, g, _dev(bf), sets, _dev(band))
+    torch.cuda.synchronize()
+    Gor = O.build_G(frames, bf)
+    for s, ab in enumerate(sets):
+        Oref, Nref = O.reduce(Gor, g, ab, bf, entries=band)
+        assert np.array_equal(Nb[s].cpu().numpy(), Nref), f"set {s}: trotter counts differ"
+        assert rel(Ob[s].cpu().numpy(), Oref) < TOL, f"set {s}"
+        ref = O.score(Oref, Nref)
+        assert abs(sc[s].item() - ref) <= TOL * abs(ref), f"set {s}"
+    # a tilted set changes which pixels are trotter pixels
+    assert not torch.equal(Nb[0], Nb[3 if B > 3 else 1])
+
+
+@pytest.mark.parametrize("case", ["small", "n512"])
+def test_score_batch_per_set_tilts_B_invariance(ssb, case, small_dataset):
+    """Per-set tilts: set s of the 8-set pass equals the same set in a shorter
+    pass and in a single-set pass, bit for bit."""
+    frames, g, base = _per_set_tilt_case(case, small_dataset)
+    bf = O.bf_indices(g, base.tilt_x_rad, base.tilt_y_rad)
+    bfd = _dev(bf)
+    band = _dev(O.band_indices(g, 0.2, 0.9))
+    G = ssb.build_G(_frames_dev(frames), g, bfd)
+    sets = _tilted_sets(base, 8, seed=53)
+    O8, N8, s8 = ssb.score_batch(G, g, bfd, sets, band)
+    for B in (2, 3, 5):
+        OB, NB, sB = ssb.score_batch(G, g, bfd, sets[:B], band)
+        assert torch.equal(OB, O8[:B]) and torch.equal(NB, N8[:B]) and torch.equal(sB, s8[:B])
+    for s in range(8):
+        O1, N1, s1 = ssb.score_batch(G, g, bfd, [sets[s]], band)
+        assert torch.equal(O1[0], O8[s]) and torch.equal(N1[0], N8[s]) and torch.equal(s1[0], s8[s])

@@ -303,6 +303,58 @@ def test_single_cosine_object_closed_form(fy0, fx0):
     assert O.score(Oq, Nq) > O.score(O2, N2)
 
 
+def _trotter_count_scalar(g, ab, bf, fy, fx):
+    """|T-(q)| + |T+(q)| by a loop over BF pixels with scalar float32 aperture
+    tests (independent of the oracle's vectorised trotters)."""
+    dq = 1.0 / (g.n * g.scan_step_A)
+    tx, ty = np.float32(ab.tilt_x_rad / g.wavelength_A), np.float32(ab.tilt_y_rad / g.wavelength_A)
+    r = g.semiangle_rad / g.wavelength_A
+    r2 = np.float32(r * r)
+    qxf, qyf = np.float32(fx * dq), np.float32(fy * dq)
+    cnt = 0
+    for pix in bf:
+        i, j = divmod(int(pix), g.det_x)
+        kx = np.float32((j - g.det_center_x) * g.det_pitch_invA)
+        ky = np.float32((i - g.det_center_y) * g.det_pitch_invA)
+        a = _aperture_scalar(kx, ky, tx, ty, r2)
+        m = _aperture_scalar(np.float32(kx - qxf), np.float32(ky - qyf), tx, ty, r2)
+        p = _aperture_scalar(np.float32(kx + qxf), np.float32(ky + qyf), tx, ty, r2)
+        cnt += int(a and (m != p))
+    return cnt
+
+
+@pytest.mark.parametrize("fy0,fx0", [(-3, 5), (4, 0), (2, 9)])
+def test_score_single_cosine_closed_form(fy0, fx0):
+    """Score over the 0.2-0.9 1/A band of the single-cosine object, in closed
+    form: O vanishes on the band except at the stored copies of +-q0, where
+    O = N(q) i eps/2 n^2, so score = (eps/2 n^2)^2 sum_{q0 copies} N(q)^2 /
+    sum_band N(q), with every N counted by the scalar brute force.  A wrong
+    denominator (band length, BF count) or a dropped square fails it."""
+    g = _geom(n=32, det=28, dk=0.17)
+    ab = _ab(C10=-80.0, C12a=20.0, C12b=-15.0, C21a=30.0, C23b=-25.0, C30=5e3,
+             C32a=-2e3, C34b=3e3, tilt_x_rad=3e-3, tilt_y_rad=-1.5e-3)
+    eps = 1e-3
+    n, h = g.n, g.n // 2 + 1
+    bf = O.bf_indices(g, ab.tilt_x_rad, ab.tilt_y_rad)
+    inten, _ = _linear_intensity_single_cosine(g, ab, bf, eps, fy0, fx0)
+    G = O.build_G(inten, bf)
+    band = O.band_indices(g, 0.2, 0.9)
+    rows, cols = band // h, band % h
+    fys = np.where(rows < n // 2, rows, rows - n)
+    # the stored copies of q0: (fy0, fx0), and (-fy0, 0) as well on the fx = 0 column
+    copies = {(fy0, fx0)} | ({(-fy0, 0)} if fx0 == 0 else set())
+    assert all(any(fy == c[0] and fx == c[1] for fy, fx in zip(fys, cols)) for c in copies)
+    Nb = np.array([_trotter_count_scalar(g, ab, bf, fy, fx) for fy, fx in zip(fys, cols)])
+    num = (eps / 2 * n * n) ** 2 * sum(
+        int(Nb[np.flatnonzero((fys == c[0]) & (cols == c[1]))[0]]) ** 2 for c in copies)
+    expect = num / float(Nb.sum())
+    Ob, Nq = O.reduce(G, g, ab, bf, entries=band)
+    assert np.array_equal(Nq, Nb)
+    assert abs(O.score(Ob, Nq) - expect) <= 1e-10 * expect
+    # the band length differs from the trotter count, so a denominator mix-up shows
+    assert len(band) != Nb.sum()
+
+
 def test_phase_image_single_cosine_closed_form():
     """From O = N i (eps/2) n^2 at one q0 and a = 1, the image is
     atan2(eps cos(2 pi q0.r), 1) exactly (C2R normalisation, -i, DC)."""

@@ -97,3 +97,20 @@ def test_noalloc_rejects_oversized_problems(ssb):
                                      fake, fake, fake, None)
     assert rc == ssb.SSB_UNSUPPORTED
     assert "16 MiB" in lib.ssb_last_error().decode()
+
+
+def test_noalloc_checks_arguments_before_the_size_limit(ssb):
+    """A NULL output or an n_bf beyond the detector is an invalid argument, as
+    for ssb_reconstruct, even on a problem too large for the fixed array."""
+    from synth import configs as C
+    lib = ssb.load()
+    a = ssb.Aberr()
+    fake = ctypes.c_void_p(1 << 20)
+    big = C.Geometry(n=1024, det_y=192, det_x=192, scan_step_A=0.373, det_pitch_invA=0.028,
+                     wavelength_A=0.019687, semiangle_rad=0.03, det_center_y=96, det_center_x=96)
+    small = C.Geometry(n=64, det_y=8, det_x=8, scan_step_A=0.373, det_pitch_invA=0.4,
+                       wavelength_A=0.019687, semiangle_rad=0.03, det_center_y=4, det_center_x=4)
+    for g, n_bf, O in ((big, 9354, None), (small, 10, None), (small, 65, fake), (big, 192 * 192 + 1, fake)):
+        rc = lib.ssb_reconstruct_noalloc(fake, ctypes.byref(ssb.to_geometry(g)), fake, n_bf, ctypes.byref(a),
+                                         O, fake, fake, None)
+        assert rc == ssb.SSB_INVALID_ARG, (g.n, n_bf, lib.ssb_last_error().decode())
