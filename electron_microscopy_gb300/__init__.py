@@ -26,7 +26,7 @@ LIB_PATH = os.path.join(_HERE, "libssb.so")
 
 SSB_OK, SSB_INVALID_ARG, SSB_UNSUPPORTED, SSB_WORKSPACE_TOO_SMALL, SSB_CUDA_ERROR = range(5)
 SSB_U16, SSB_F32 = 0, 1
-OP_BUILD, OP_RECON, OP_SCORE, OP_MOMENTS = 0, 1, 2, 3
+OP_BUILD, OP_RECON, OP_SCORE, OP_MOMENTS, OP_PHASE = 0, 1, 2, 3, 4
 MAX_SETS = 8
 
 STATUS_NAMES = {0: "SSB_OK", 1: "SSB_INVALID_ARG", 2: "SSB_UNSUPPORTED",
@@ -36,7 +36,7 @@ EXPORTED = ("ssb_bf_indices", "ssb_band_indices", "ssb_workspace_bytes", "ssb_bu
             "ssb_reconstruct", "ssb_score_batch", "ssb_last_error", "ssb_launch_count",
             "ssb_reconstruct_noalloc", "ssb_build_G_host", "ssb_build_G_host_bytes",
             "ssb_compact_G16", "ssb_compact_band", "ssb_reconstruct_g", "ssb_score_batch_g",
-            "ssb_phase_moments")
+            "ssb_phase_moments", "ssb_reconstruct_sums", "ssb_phase_from_sums")
 
 G_C64, G_SN16 = 0, 1
 
@@ -121,11 +121,14 @@ def load(path: str | None = None):
     lib.ssb_score_batch_g.argtypes = [S_p, G_p, c_vp, c_int, A_p, c_int, c_vp, c_int, c_vp, c_vp, c_vp,
                                       c_vp, c_size, c_vp]
     lib.ssb_phase_moments.argtypes = [S_p, G_p, c_vp, c_int, A_p, c_vp, c_vp, c_vp, c_size, c_vp]
+    lib.ssb_reconstruct_sums.argtypes = [c_vp, G_p, c_vp, c_int, A_p, c_vp, c_vp, c_vp, c_vp, c_size, c_vp]
+    lib.ssb_phase_from_sums.argtypes = [c_vp, c_vp, c_vp, c_int, G_p, c_vp, c_vp, c_size, c_vp]
     lib.ssb_last_error.restype = ctypes.c_char_p
     lib.ssb_launch_count.restype = ctypes.c_longlong
     for fn in ("ssb_bf_indices", "ssb_band_indices", "ssb_build_G", "ssb_build_G_host", "ssb_reconstruct",
                "ssb_score_batch", "ssb_reconstruct_noalloc", "ssb_compact_G16", "ssb_compact_band",
-               "ssb_reconstruct_g", "ssb_score_batch_g", "ssb_phase_moments"):
+               "ssb_reconstruct_g", "ssb_score_batch_g", "ssb_phase_moments", "ssb_reconstruct_sums",
+               "ssb_phase_from_sums"):
         getattr(lib, fn).restype = c_int
     _lib = lib
     return lib
@@ -301,6 +304,43 @@ def reconstruct(G, geom, bf_idx_dev, aberr, O=None, N=None, phase=None, ws=None,
                                                   ctypes.byref(a), _ptr(O), _ptr(N), _ptr(phase),
                                                   ws.ptr(), ws.nbytes, _stream(stream)))
     return O, N, phase
+
+
+def reconstruct_sums(G, geom, bf_idx_dev, aberr, O=None, N=None, g0_sum=None, ws=None, stream=None):
+    """One shard of a reconstruction: the raw sums (O complex64 [n, n/2+1],
+    N int32 [n, n/2+1]) over this shard's BF pixels and sum_k Re G(0,k)
+    (float64 [1]).  Add the shards' results, then call phase_from_sums."""
+    import torch
+    lib = load()
+    g = to_geometry(geom)
+    a = to_aberr(aberr)
+    n_bf = int(bf_idx_dev.numel())
+    n, h = g.n, g.n // 2 + 1
+    dev = G.device
+    O = torch.empty((n, h), dtype=torch.complex64, device=dev) if O is None else O
+    N = torch.empty((n, h), dtype=torch.int32, device=dev) if N is None else N
+    g0_sum = torch.empty((1,), dtype=torch.float64, device=dev) if g0_sum is None else g0_sum
+    if ws is None:
+        ws = Workspace(workspace_bytes(g, n_bf, OP_RECON), dev)
+    _check("ssb_reconstruct_sums", lib.ssb_reconstruct_sums(
+        _ptr(G), ctypes.byref(g), _ptr(bf_idx_dev), n_bf, ctypes.byref(a), _ptr(O), _ptr(N), _ptr(g0_sum),
+        ws.ptr(), ws.nbytes, _stream(stream)))
+    return O, N, g0_sum
+
+
+def phase_from_sums(O, N, g0_sum, n_bf_total, geom, phase=None, ws=None, stream=None):
+    """Phase image (float32 [n, n]) from summed shard results."""
+    import torch
+    lib = load()
+    g = to_geometry(geom)
+    dev = O.device
+    phase = torch.empty((g.n, g.n), dtype=torch.float32, device=dev) if phase is None else phase
+    if ws is None:
+        ws = Workspace(workspace_bytes(g, 1, OP_PHASE), dev)
+    _check("ssb_phase_from_sums", lib.ssb_phase_from_sums(
+        _ptr(O), _ptr(N), _ptr(g0_sum), int(n_bf_total), ctypes.byref(g), _ptr(phase), ws.ptr(), ws.nbytes,
+        _stream(stream)))
+    return phase
 
 
 def score_batch(G, geom, bf_idx_dev, sets, band_dev, O=None, N=None, score=None, ws=None, stream=None):

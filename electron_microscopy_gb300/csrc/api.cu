@@ -144,6 +144,12 @@ static WsLayout layout(const ssb_geometry* g, int n_bf, int op, int B, int nq) {
         L.total = off;
         return L;
     }
+    if (op == SSB_OP_PHASE) {  // the complex-to-real intermediate
+        L.Y = off;
+        off += align256((size_t)n * H * sizeof(float2));
+        L.total = off;
+        return L;
+    }
     if (op == SSB_OP_MOMENTS) {
         L.ktab = off;
         off += align256((size_t)n_bf * sizeof(float4));
@@ -307,7 +313,9 @@ size_t ssb_workspace_bytes(const ssb_geometry* geom, int n_bf, int op, int B, in
     if (check_geom(geom) != SSB_OK) return 0;
     if (n_bf < 1) return 0;
     if (op == SSB_OP_SCORE && (B < 1 || B > SSB_MAX_SETS || nq < 1)) return 0;
-    if (op != SSB_OP_BUILD && op != SSB_OP_RECON && op != SSB_OP_SCORE && op != SSB_OP_MOMENTS) return 0;
+    if (op != SSB_OP_BUILD && op != SSB_OP_RECON && op != SSB_OP_SCORE && op != SSB_OP_MOMENTS &&
+        op != SSB_OP_PHASE)
+        return 0;
     return layout(geom, n_bf, op, B, nq).total;
 }
 
@@ -340,7 +348,7 @@ int ssb_build_G(const void* frames, int dtype, const ssb_geometry* geom, const i
 // detector (rows r0.., columns c0..), staged in the workspace ahead of the
 // build workspace
 struct HostLayout {
-    int r0 = 0, rows = 0, c0 = 0, cols = 0;
+    int r0 = 0, rows = 0, c0 = 0, cols = 0, pitch = 0;
     size_t crop = 0, idx = 0, build = 0, total = 0;
 };
 
@@ -361,14 +369,20 @@ static int host_layout(const ssb_geometry* geom, int dtype, const int32_t* bf_ho
         clo = c < clo ? c : clo;
         chi = c > chi ? c : chi;
     }
+    // the box starts on an even column (kept so that any build that pairs
+    // the two pixels of a 4-byte detector word sees the same words)
+    if (chi - clo + 1 < geom->det_x) clo &= ~1;
     ssb_geometry crop = *geom;
     crop.det_y = rhi - rlo + 1;
-    crop.det_x = chi - clo + 1;
     const size_t es = dtype == SSB_U16 ? 2 : 4;
     H->r0 = rlo;
     H->rows = crop.det_y;
     H->c0 = clo;
-    H->cols = crop.det_x;
+    H->cols = chi - clo + 1;
+    // staged rows are padded to a multiple of 16 bytes (whole detector rows
+    // are copied unpadded), so the build can read them in 16-byte pieces
+    H->pitch = H->cols == geom->det_x ? geom->det_x : (int)(((size_t)H->cols * es + 15) / 16 * 16 / es);
+    crop.det_x = H->pitch;
     H->crop = 0;
     H->idx = align256((size_t)geom->n * geom->n * crop.det_y * crop.det_x * es);
     H->build = H->idx + align256((size_t)n_bf * sizeof(int32_t));
@@ -405,7 +419,7 @@ int ssb_build_G_host(const void* frames_host, int dtype, const ssb_geometry* geo
         cudaMemcpy3DParms p = {};
         p.srcPtr = make_cudaPitchedPtr(const_cast<void*>(frames_host), row_bytes, row_bytes, (size_t)geom->det_y);
         p.srcPos = make_cudaPos((size_t)H.c0 * es, (size_t)H.r0, 0);
-        p.dstPtr = make_cudaPitchedPtr(at<char>(ws, H.crop), (size_t)H.cols * es, (size_t)H.cols * es,
+        p.dstPtr = make_cudaPitchedPtr(at<char>(ws, H.crop), (size_t)H.pitch * es, (size_t)H.cols * es,
                                        (size_t)H.rows);
         p.dstPos = make_cudaPos(0, 0, 0);
         p.extent = make_cudaExtent((size_t)H.cols * es, (size_t)H.rows, (size_t)geom->n * geom->n);
@@ -414,11 +428,11 @@ int ssb_build_G_host(const void* frames_host, int dtype, const ssb_geometry* geo
     }
     if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy of the bright-field box");
     int32_t* idx = at<int32_t>(ws, H.idx);
-    if ((e = launch_crop_idx(bf_idx_dev, n_bf, geom->det_x, H.r0, H.c0, H.cols, idx, st)) != cudaSuccess)
+    if ((e = launch_crop_idx(bf_idx_dev, n_bf, geom->det_x, H.r0, H.c0, H.pitch, idx, st)) != cudaSuccess)
         return cuda_fail(e, "index remap");
     ssb_geometry crop = *geom;
     crop.det_y = H.rows;
-    crop.det_x = H.cols;
+    crop.det_x = H.pitch;
     return ssb_build_G(at<char>(ws, H.crop), dtype, &crop, idx, n_bf, G_dev, at<char>(ws, H.build),
                        ws_bytes - H.build, stream);
 }
@@ -481,6 +495,55 @@ static int reconstruct_impl(const ssb_gstore* store, const ssb_geometry* geom, c
         return rc;
     if ((e = launch_phase(static_cast<const float2*>(O_dev), N_dev, at<double>(ws, Lw.dcpart),
                           (n_bf + 255) / 256, n_bf, n, at<float2>(ws, Lw.Y), tw, phase_dev, st)) != cudaSuccess)
+        return cuda_fail(e, "phase");
+    g_err[0] = 0;
+    return SSB_OK;
+}
+
+int ssb_reconstruct_sums(const void* G_dev, const ssb_geometry* geom, const int32_t* bf_idx_dev, int n_bf,
+                         const ssb_aberr* set, void* O_dev, int32_t* N_dev, double* g0_sum_dev, void* ws,
+                         size_t ws_bytes, void* stream) {
+    int rc;
+    GView gv{};
+    const ssb_gstore store = c64_store(G_dev);
+    if (!g0_sum_dev) return fail(SSB_INVALID_ARG, "g0_sum must not be NULL");
+    // the image is not formed here: any non-null pointer stands in for it
+    if ((rc = check_recon_args(&store, geom, bf_idx_dev, n_bf, set, O_dev, N_dev,
+                               reinterpret_cast<const float*>(g0_sum_dev), &gv)) != SSB_OK)
+        return rc;
+    const WsLayout Lw = layout(geom, n_bf, SSB_OP_RECON, 1, 0);
+    if ((rc = check_ws(ws, ws_bytes, Lw.total)) != SSB_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    SetBatch sb{};
+    sb.B = 1;
+    sb.r2 = aperture_r2(geom);
+    sb.s[0] = set_params(geom, set);
+    const int n = geom->n, nq = n * (n / 2 + 1);
+    if ((rc = run_reduction(gv, geom, bf_idx_dev, n_bf, sb, nullptr, nq, static_cast<float2*>(O_dev), N_dev,
+                            ws, Lw, 1, st)) != SSB_OK)
+        return rc;
+    cudaError_t e;
+    if ((e = launch_dc_total(at<double>(ws, Lw.dcpart), (n_bf + 255) / 256, g0_sum_dev, st)) != cudaSuccess)
+        return cuda_fail(e, "G(0,k) sum");
+    g_err[0] = 0;
+    return SSB_OK;
+}
+
+int ssb_phase_from_sums(const void* O_dev, const int32_t* N_dev, const double* g0_sum_dev, int n_bf_total,
+                        const ssb_geometry* geom, float* phase_dev, void* ws, size_t ws_bytes, void* stream) {
+    int rc;
+    if ((rc = check_geom(geom)) != SSB_OK) return rc;
+    if (!O_dev || !N_dev || !g0_sum_dev || !phase_dev)
+        return fail(SSB_INVALID_ARG, "O, N, g0_sum and phase must not be NULL");
+    if (n_bf_total < 1) return fail(SSB_INVALID_ARG, "n_bf_total=%d must be >= 1", n_bf_total);
+    const WsLayout Lw = layout(geom, 1, SSB_OP_PHASE, 1, 0);
+    if ((rc = check_ws(ws, ws_bytes, Lw.total)) != SSB_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    float2* tw = at<float2>(ws, Lw.tw);
+    cudaError_t e;
+    if ((e = launch_twiddles(tw, geom->n, st)) != cudaSuccess) return cuda_fail(e, "twiddles");
+    if ((e = launch_phase(static_cast<const float2*>(O_dev), N_dev, g0_sum_dev, 1, n_bf_total, geom->n,
+                          at<float2>(ws, Lw.Y), tw, phase_dev, st)) != cudaSuccess)
         return cuda_fail(e, "phase");
     g_err[0] = 0;
     return SSB_OK;

@@ -421,6 +421,8 @@ cudaError_t launch_finalize(const float2* Opart, const int* Npart, int nsplit, i
 cudaError_t launch_phase(const float2* O, const int32_t* N, const double* dcpart, int nsplit,
                          int n_bf, int n, float2* Y, const float2* tw, float* phase,
                          cudaStream_t st);
+// total[0] = sum of part[0..nparts) in that order (float64)
+cudaError_t launch_dc_total(const double* part, int nparts, double* total, cudaStream_t st);
 cudaError_t launch_score(const float2* O, const int32_t* N, int B, int nq, double* score,
                          cudaStream_t st);
 // per-BF phase moments (moments.cu): Y holds moments_chunk_bytes(n), part

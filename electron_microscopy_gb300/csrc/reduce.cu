@@ -539,6 +539,23 @@ cudaError_t launch_phase(const float2* O, const int32_t* Nn, const double* dcpar
 }
 
 // ---------------------------------------------------------------------------
+// sum_k Re G(0,k) from the per-256-pixel partials, in the order the image
+// kernel adds them (so one shard holding every pixel reproduces its offset)
+// ---------------------------------------------------------------------------
+__global__ void ssb_dc_total(const double* __restrict__ part, int nparts, double* __restrict__ total) {
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    double dc = 0.0;
+    for (int sp = 0; sp < nparts; ++sp) dc += part[sp];
+    total[0] = dc;
+}
+
+cudaError_t launch_dc_total(const double* part, int nparts, double* total, cudaStream_t st) {
+    ssb_dc_total<<<1, 32, 0, st>>>(part, nparts, total);
+    count_launch();
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
 // score_s = sum_q |O_s(q)|^2 / sum_q N_s(q), one block per set, float64 sums
 // ---------------------------------------------------------------------------
 __global__ void ssb_score(const float2* __restrict__ O, const int32_t* __restrict__ Nn, int nq,

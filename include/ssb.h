@@ -100,7 +100,9 @@ typedef enum ssb_status {
     SSB_CUDA_ERROR = 4            /* a launch failed; see ssb_last_error()             */
 } ssb_status;
 
-typedef enum ssb_op { SSB_OP_BUILD = 0, SSB_OP_RECON = 1, SSB_OP_SCORE = 2, SSB_OP_MOMENTS = 3 } ssb_op;
+typedef enum ssb_op {
+    SSB_OP_BUILD = 0, SSB_OP_RECON = 1, SSB_OP_SCORE = 2, SSB_OP_MOMENTS = 3, SSB_OP_PHASE = 4
+} ssb_op;
 
 #define SSB_MAX_SETS 8
 #define SSB_MIN_N 8
@@ -130,9 +132,11 @@ int ssb_band_indices(const ssb_geometry* geom, double qmin, double qmax,
 
 /*
  * Bytes of device workspace an operation needs (0 on invalid arguments).
- * op = SSB_OP_BUILD, SSB_OP_RECON (B ignored, nq ignored), SSB_OP_SCORE
- * (B sets over nq band entries) or SSB_OP_MOMENTS (B, nq ignored).  The
- * workspace must be 256-byte aligned.
+ * op = SSB_OP_BUILD, SSB_OP_RECON (ssb_reconstruct and ssb_reconstruct_sums;
+ * B ignored, nq ignored), SSB_OP_SCORE (B sets over nq band entries),
+ * SSB_OP_MOMENTS (B, nq ignored) or SSB_OP_PHASE (ssb_phase_from_sums; n_bf,
+ * B, nq ignored but n_bf must be >= 1).  The workspace must be 256-byte
+ * aligned.
  */
 size_t ssb_workspace_bytes(const ssb_geometry* geom, int n_bf, int op, int B, int nq);
 
@@ -194,6 +198,38 @@ int ssb_reconstruct(const void* G_dev, const ssb_geometry* geom,
                     const int32_t* bf_idx_dev, int n_bf, const ssb_aberr* set,
                     void* O_dev, int32_t* N_dev, float* phase_dev,
                     void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * A reconstruction split over shards of the BF pixels (one shard per GPU, or
+ * any partition of the BF list).  Every quantity the image needs is a sum over
+ * BF pixels ("Tilt-corrected SSB on CUDA", section "Where the time went": the
+ * reduction is a sum over k; "Historical WebGPU G(q,k) memory experiment",
+ * section "Implementation": G is built per BF pixel), so each shard reduces
+ * its own pixels and the shards' results are added (an all-reduce across
+ * GPUs) before one call forms the image.
+ *
+ * ssb_reconstruct_sums: for the n_bf pixels given (G_dev holds their half
+ * planes, [n_bf][n][n/2+1]; bf_idx_dev their detector indices), writes the
+ * raw sums O_dev (complex64 [n][n/2+1]) and N_dev (int32 [n][n/2+1]) exactly
+ * as ssb_reconstruct does, and g0_sum_dev[0] (float64) = sum_k Re G(0,k) over
+ * these pixels.  Workspace: ssb_workspace_bytes(..., SSB_OP_RECON, ...).
+ * Errors as ssb_reconstruct (g0_sum_dev must not be NULL).
+ *
+ * ssb_phase_from_sums: phase_dev (float32 [n][n]) from the shards' summed O,
+ * N and G(0,k) sum, with n_bf_total the number of BF pixels over all shards
+ * (a = g0_sum / n_bf_total / n^2, the rest as ssb_reconstruct).  Workspace:
+ * ssb_workspace_bytes(geom, 1, SSB_OP_PHASE, 1, 1).  With one shard holding
+ * every pixel, the two calls give ssb_reconstruct's O, N and phase bit for
+ * bit.  Errors: SSB_INVALID_ARG for a NULL pointer or n_bf_total < 1.
+ */
+int ssb_reconstruct_sums(const void* G_dev, const ssb_geometry* geom,
+                         const int32_t* bf_idx_dev, int n_bf, const ssb_aberr* set,
+                         void* O_dev, int32_t* N_dev, double* g0_sum_dev,
+                         void* ws, size_t ws_bytes, void* stream);
+
+int ssb_phase_from_sums(const void* O_dev, const int32_t* N_dev, const double* g0_sum_dev,
+                        int n_bf_total, const ssb_geometry* geom, float* phase_dev,
+                        void* ws, size_t ws_bytes, void* stream);
 
 /*
  * Batched scoring of B aberration sets (sets: host array of B) over a band

@@ -168,15 +168,17 @@ def test_no_launches_from_failed_checks(lib):
 
 
 def test_build_G_host_bytes(lib):
-    """Workspace of the host-input build: the BF bounding box of every frame,
-    the remapped index list and the build workspace of the cropped detector."""
+    """Workspace of the host-input build: the BF bounding box of every frame
+    (rows padded to a multiple of 16 bytes), the remapped index list and the
+    build workspace of the cropped detector."""
     g = C.geometry(C.WORKLOADS["full"])
     bf = O.bf_indices(g)
     rows, cols = bf // g.det_x, bf % g.det_x
     r0, r1, c0, c1 = int(rows.min()), int(rows.max()), int(cols.min()), int(cols.max())
-    crop = C.Geometry(**{**g.__dict__, "det_y": r1 - r0 + 1, "det_x": c1 - c0 + 1})
+    pitch = (c1 - (c0 & ~1) + 1 + 7) // 8 * 8
+    crop = C.Geometry(**{**g.__dict__, "det_y": r1 - r0 + 1, "det_x": pitch})
     a256 = lambda x: (x + 255) // 256 * 256  # noqa: E731
-    want = (a256(g.n * g.n * (r1 - r0 + 1) * (c1 - c0 + 1) * 2) + a256(len(bf) * 4)
+    want = (a256(g.n * g.n * (r1 - r0 + 1) * pitch * 2) + a256(len(bf) * 4)
             + ssb.workspace_bytes(crop, len(bf), ssb.OP_BUILD))
     assert ssb.build_G_host_bytes(g, bf, ssb.SSB_U16) == want
     # the full workload's disk spans rows and columns 42..150 of 192: 32 % of the frame bytes cross the link
