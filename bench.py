@@ -32,11 +32,43 @@ if ROOT not in sys.path:
 
 METRIC = "ms per SSB recon + G-build HBM GB/s (512^2 scan, 192^2 det, ~9.3k BF px)"
 
-# DRAM bytes (read + write) of one ssb_build_G call on the full workload, from
-# the ncu capture summarised in profiles/build_traffic_full.md, valid for the
-# build kernels' source with this SHA-256 prefix only (null otherwise)
-BUILD_TRAFFIC = {"plane_cu_sha256": "b845ca1145fa8310", "bytes": 26.80e9}
 L2_BYTES = 129 * 1024 * 1024
+
+
+def gpu_numa_node(index):
+    """NUMA node of GPU `index` (sysfs of its PCI function), or None."""
+    try:
+        out = subprocess.run(["nvidia-smi", f"--id={index}", "--query-gpu=pci.bus_id", "--format=csv,noheader"],
+                             capture_output=True, text=True, timeout=30).stdout.strip()
+        bus = out.split()[0].lower()
+        dom, rest = bus.split(":", 1)
+        path = f"/sys/bus/pci/devices/{dom[-4:]}:{rest}/numa_node"
+        node = int(open(path).read().strip())
+        return node if node >= 0 else None
+    except (OSError, ValueError, IndexError, subprocess.SubprocessError):
+        return None
+
+
+def bind_to_node(node):
+    """Restrict this process to the CPUs of NUMA node `node` (so that pinned
+    host buffers allocated afterwards are first touched there).  Returns the
+    CPU list used, or None."""
+    try:
+        text = open(f"/sys/devices/system/node/node{node}/cpulist").read().strip()
+    except OSError:
+        return None
+    cpus = set()
+    for part in text.split(","):
+        if "-" in part:
+            a, b = part.split("-")
+            cpus.update(range(int(a), int(b) + 1))
+        elif part:
+            cpus.add(int(part))
+    cpus &= os.sched_getaffinity(0)
+    if not cpus:
+        return None
+    os.sched_setaffinity(0, cpus)
+    return sorted(cpus)
 
 
 def parse():
@@ -372,12 +404,10 @@ def run_ours(args, ws, rank, local, pg):
         hbm = 6800.0
         peak_src = "fallback"
     achieved = bytes_build / (build_ms * 1e-3) / 1e9
+    # DRAM counters are taken with ncu on the mid workload only (a full-size
+    # multi-kernel capture is outside the profiling bounds), so no per-launch
+    # traffic of the full build is claimed here
     traffic = None
-    if args.workload == "full":
-        import hashlib
-        src = open(os.path.join(ROOT, "electron_microscopy_gb300", "csrc", "plane.cu"), "rb").read()
-        if hashlib.sha256(src).hexdigest().startswith(BUILD_TRAFFIC["plane_cu_sha256"]):
-            traffic = BUILD_TRAFFIC["bytes"]
 
     # end to end through the public API with host buffers: the frames stay in
     # pinned host memory and ssb_build_G_host copies the bright-field box of
@@ -387,8 +417,13 @@ def run_ours(args, ws, rank, local, pg):
     # would run.
     e2e = None
     if not args.no_e2e:
+        vis_e = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        numa = gpu_numa_node(vis_e.split(",")[local] if vis_e else local)
+        cpus_before = os.sched_getaffinity(0)
+        bound = bind_to_node(numa) if numa is not None else None
         host = torch.empty(frames.shape, dtype=frames.dtype, pin_memory=True)
-        host.copy_(frames)
+        host.copy_(frames)  # first touch on the GPU's node
+        os.sched_setaffinity(0, cpus_before)
         code = ssb.SSB_U16 if frames.element_size() == 2 else ssb.SSB_F32
         r_bf, c_bf = bf // geom.det_x, bf % geom.det_x
         box = (int(r_bf.min()), int(r_bf.max()), int(c_bf.min()), int(c_bf.max()))
@@ -436,8 +471,37 @@ def run_ours(args, ws, rank, local, pg):
         eb.record(t_stream)
         torch.cuda.synchronize()
         e2e_ms = allmax(pg, ea.elapsed_time(eb) / E, dev)
+        # one call on its own (no pipelining): copy in, compute, results out
+        L0 = lanes[0]
+        ec, ed = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        lat = []
+        for _ in range(2):
+            torch.cuda.synchronize()
+            ec.record(L0["stream"])
+            e2e_step(L0)
+            ed.record(L0["stream"])
+            torch.cuda.synchronize()
+            lat.append(ec.elapsed_time(ed))
+        # the host link's ceiling in this run: one contiguous pinned copy of
+        # the same number of bytes
+        nel = h2d // frames.element_size()
+        src_h = host.view(-1)[:nel]
+        dst_d = torch.empty(nel, dtype=frames.dtype, device=dev)
+        for _ in range(2):
+            dst_d.copy_(src_h, non_blocking=True)
+        ef, eg = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ef.record()
+        dst_d.copy_(src_h, non_blocking=True)
+        eg.record()
+        torch.cuda.synchronize()
+        link_GBs = h2d / (ef.elapsed_time(eg) * 1e-3) / 1e9
+        del dst_d
         e2e = {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": ph.numel() * 4 + sc.numel() * 8, "steps": E,
+               "latency_ms": min(lat), "link_GBs": link_GBs,
+               "link_frac": h2d / (e2e_ms * 1e-3) / 1e9 / link_GBs,
+               "link": "one contiguous pinned host-to-device copy of the step's bytes, timed in this run",
+               "host_numa_node": numa, "host_cpus_bound": len(bound) if bound else None,
                "call": f"ssb_build_G_host (detector box rows {box[0]}..{box[1]}, columns {box[2]}..{box[3]} of "
                        f"{geom.det_y}x{geom.det_x}) + ssb_reconstruct + ssb_score_batch, phase and scores to host",
                "pipelining": "two streams alternate steps: the host-to-device copy of step i+1 overlaps step i"}
@@ -465,11 +529,14 @@ def run_ours(args, ws, rank, local, pg):
 
     # the other stages against their binding units: the reconstruction streams
     # all of G (HBM); the 8-set scoring pass does one sincos (2 transcendental
-    # ops) per active term, against the XU rate of 16 results per clock per SM
-    # at the median SM clock sampled under load
+    # results) per active term, against the sin/cos rate measured here by the
+    # library's probe kernel (also the float32 FMA rate, context for the FFT)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     clk_mhz = (clk or {}).get("sm_mhz") or 2070.0
-    xu_peak = 16.0 * sms * clk_mhz * 1e6
+    with torch.cuda.stream(stream):
+        rates = ssb.peak_rates(dev, stream=stream)
+    xu_peak = rates["sincos_per_s"]
+    fp32_peak = rates["fma_flops_per_s"]
     xu_ach = 2.0 * terms / (score_ms * 1e-3)
     def timed(run, reps=10, warm=3):
         """mean ms of `run` over `reps` calls, CUDA events on the launching stream"""
@@ -571,8 +638,13 @@ def run_ours(args, ws, rank, local, pg):
                         "algorithmic_bytes": bytes_recon},
         "score": {"bound": "xu", "achieved": xu_ach / 1e9, "peak": xu_peak / 1e9, "unit": "Gop/s",
                   "frac": xu_ach / xu_peak, "ops": 2 * terms,
-                  "peak_source": f"derived: 16 sin/cos per clock per SM x {sms} SMs x {clk_mhz:.0f} MHz",
+                  "peak_source": "measured in this run: ssb_peak_sincos (8 independent __sincosf chains per "
+                                 f"thread, {rates['blocks']} CTAs x 256 threads)",
+                  "derived_peak": 16.0 * sms * clk_mhz * 1e6 / 1e9,
+                  "derived_source": f"16 sin/cos per clock per SM x {sms} SMs x {clk_mhz:.0f} MHz",
                   "hbm_frac": bytes_score / (score_ms * 1e-3) / 1e9 / hbm},
+        "build_fp32": {"bound": "fp32 (context)", "peak": fp32_peak / 1e12, "unit": "TFLOP/s",
+                       "peak_source": "measured in this run: ssb_peak_fma (8 independent FMA chains per thread)"},
     }
 
     if rank != 0:

@@ -36,7 +36,8 @@ EXPORTED = ("ssb_bf_indices", "ssb_band_indices", "ssb_workspace_bytes", "ssb_bu
             "ssb_reconstruct", "ssb_score_batch", "ssb_last_error", "ssb_launch_count",
             "ssb_reconstruct_noalloc", "ssb_build_G_host", "ssb_build_G_host_bytes",
             "ssb_compact_G16", "ssb_compact_band", "ssb_reconstruct_g", "ssb_score_batch_g",
-            "ssb_phase_moments", "ssb_reconstruct_sums", "ssb_phase_from_sums")
+            "ssb_phase_moments", "ssb_reconstruct_sums", "ssb_phase_from_sums", "ssb_peak_sincos",
+            "ssb_peak_fma")
 
 G_C64, G_SN16 = 0, 1
 
@@ -123,12 +124,14 @@ def load(path: str | None = None):
     lib.ssb_phase_moments.argtypes = [S_p, G_p, c_vp, c_int, A_p, c_vp, c_vp, c_vp, c_size, c_vp]
     lib.ssb_reconstruct_sums.argtypes = [c_vp, G_p, c_vp, c_int, A_p, c_vp, c_vp, c_vp, c_vp, c_size, c_vp]
     lib.ssb_phase_from_sums.argtypes = [c_vp, c_vp, c_vp, c_int, G_p, c_vp, c_vp, c_size, c_vp]
+    lib.ssb_peak_sincos.argtypes = [c_vp, c_int, c_int, c_vp]
+    lib.ssb_peak_fma.argtypes = [c_vp, c_int, c_int, c_vp]
     lib.ssb_last_error.restype = ctypes.c_char_p
     lib.ssb_launch_count.restype = ctypes.c_longlong
     for fn in ("ssb_bf_indices", "ssb_band_indices", "ssb_build_G", "ssb_build_G_host", "ssb_reconstruct",
                "ssb_score_batch", "ssb_reconstruct_noalloc", "ssb_compact_G16", "ssb_compact_band",
                "ssb_reconstruct_g", "ssb_score_batch_g", "ssb_phase_moments", "ssb_reconstruct_sums",
-               "ssb_phase_from_sums"):
+               "ssb_phase_from_sums", "ssb_peak_sincos", "ssb_peak_fma"):
         getattr(lib, fn).restype = c_int
     _lib = lib
     return lib
@@ -341,6 +344,32 @@ def phase_from_sums(O, N, g0_sum, n_bf_total, geom, phase=None, ws=None, stream=
         _ptr(O), _ptr(N), _ptr(g0_sum), int(n_bf_total), ctypes.byref(g), _ptr(phase), ws.ptr(), ws.nbytes,
         _stream(stream)))
     return phase
+
+
+def peak_rates(device=None, iters=(4096, 32768), stream=None):
+    """Measured rates on the current device: transcendental results per second
+    (one __sincosf = 2) and float32 flops per second (FMA = 2), from the
+    library's probe kernels timed with CUDA events on `stream`."""
+    import torch
+    lib = load()
+    dev = torch.device("cuda") if device is None else device
+    props = torch.cuda.get_device_properties(dev)
+    blocks = props.multi_processor_count * 8
+    out = torch.zeros(1, dtype=torch.float32, device=dev)
+    st = torch.cuda.current_stream(dev) if stream is None else stream
+    res = {}
+    for (name, fn), it in zip((("sincos_per_s", lib.ssb_peak_sincos), ("fma_flops_per_s", lib.ssb_peak_fma)),
+                              iters):
+        for _ in range(2):  # warm-up
+            _check(fn.__name__, fn(_ptr(out), blocks, it, _stream(st)))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        _check(fn.__name__, fn(_ptr(out), blocks, it, _stream(st)))
+        e1.record(st)
+        e1.synchronize()
+        res[name] = 2.0 * 8 * 256 * blocks * it / (e0.elapsed_time(e1) * 1e-3)
+    res["blocks"], res["iters"] = blocks, list(iters)
+    return res
 
 
 def score_batch(G, geom, bf_idx_dev, sets, band_dev, O=None, N=None, score=None, ws=None, stream=None):

@@ -16,7 +16,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libssb.so")
 
-SOURCES = ("api.cu", "build.cu", "plane.cu", "reduce.cu", "compact.cu", "moments.cu", "noalloc.cu")
+SOURCES = ("api.cu", "build.cu", "plane.cu", "reduce.cu", "compact.cu", "moments.cu", "noalloc.cu", "peaks.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-I", INCLUDE,
          "-Xcompiler", "-fPIC,-ffp-contract=off,-O2"]
@@ -43,7 +43,7 @@ def build(verbose: bool = False, force: bool = False, extra_flags: list[str] | N
     os.makedirs(BUILD, exist_ok=True)
     exe = nvcc()
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cuh")]
-    headers.append(os.path.join(INCLUDE, "ssb.h"))
+    headers += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
     flags = FLAGS + list(extra_flags or [])
     jobs = []
     objs = []

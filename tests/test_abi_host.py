@@ -24,9 +24,13 @@ def lib():
 
 
 def _declared_functions():
-    text = open(os.path.join(ROOT, "include", "ssb.h")).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(ssb_[A-Za-z_0-9]+)\s*\(", text)))
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in sorted(os.listdir(inc)):
+        if f.endswith(".h"):
+            text = re.sub(r"/\*.*?\*/", "", open(os.path.join(inc, f)).read(), flags=re.S)
+            names |= set(re.findall(r"\b(ssb_[A-Za-z_0-9]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_the_binding_names():
@@ -158,6 +162,14 @@ def test_error_codes_reconstruct_and_score(lib):
     assert rc == ssb.SSB_INVALID_ARG
     rc = lib.ssb_score_batch(FAKE, ctypes.byref(g), FAKE, 10, sets, 2, FAKE, 5, FAKE, FAKE, FAKE, FAKE, 64, None)
     assert rc == ssb.SSB_WORKSPACE_TOO_SMALL
+
+
+def test_peak_probes_reject_bad_arguments(lib):
+    before = lib.ssb_launch_count()
+    assert lib.ssb_peak_sincos(None, 4, 4, None) == ssb.SSB_INVALID_ARG
+    assert lib.ssb_peak_fma(FAKE, 0, 4, None) == ssb.SSB_INVALID_ARG
+    assert lib.ssb_peak_fma(FAKE, 4, 0, None) == ssb.SSB_INVALID_ARG
+    assert lib.ssb_launch_count() == before
 
 
 def test_no_launches_from_failed_checks(lib):
