@@ -364,6 +364,70 @@ def score_sets(G, geom, sets, bf_idx, band):
 
 
 # ----------------------------------------------------------------------------
+# depth-spread ("thick") fit: the weights averaged over a defocus spread
+# ----------------------------------------------------------------------------
+# Source: "Tilt-corrected SSB on CUDA: fit and preview speed", sections
+# "Changes" (the fit kernel at depth 136 A and at depth 0; per (k, q, set) term
+# two sincos and two sin at depth, the transcendental pipe busiest) and
+# "Results" (a depth spread is one of the fitted parameters); "Where the 9 s of
+# regularized preparation goes", list item 2 ("chi, sinc and phase factor" of
+# a transfer term, evaluated only inside the lens).  The pages never write
+# the depth model out.
+# READING depth model: the probe's defocus is spread uniformly over a slab of
+# thickness t centred on the set's C10 (z in [-t/2, t/2], defocus C10 + z);
+# defocus enters chi(v) as pi lambda C10 |v|^2 (radians), so the transfer of a
+# trotter pixel, averaged over the slab, is its depth-0 value times the real
+# factor avg_z exp(i pi lambda z D) = sinc(pi lambda t D / 2), sinc(x) =
+# sin(x)/x, with D = |v_k|^2 - |v_{k-q}|^2 on T- and |v_k|^2 - |v_{k+q}|^2 on T+
+# (v = k - k_t).
+# READING weight: the fit weights each trotter term by the depth-0 weight
+# times that factor (the matched filter of the averaged transfer); N(q) still
+# counts trotter pixels, and the score is sum |O|^2 / sum N as at depth 0.
+# t = 0 gives the depth-0 weights exactly.
+
+def depth_factor(geom, ab, bf_idx, qx, qy, tminus, tplus, depth_A):
+    """Real (Nq, N_bf) factor sinc(pi lambda t D / 2) on T-/T+ (1 elsewhere),
+    float64; depth_A = t (Angstrom, >= 0)."""
+    _, _, det_x, _, _, lam, *_ = _g(geom)
+    a = _ab(ab)
+    ktx, kty = a[12] / lam, a[13] / lam
+    idx = np.asarray(bf_idx, dtype=np.int64)
+    kx, ky = det_k(geom, idx // det_x, idx % det_x)
+    vkx, vky = (kx - ktx)[None, :], (ky - kty)[None, :]
+    qx = np.asarray(qx, dtype=np.float64)[:, None]
+    qy = np.asarray(qy, dtype=np.float64)[:, None]
+    vk2 = vkx * vkx + vky * vky
+    dm = vk2 - ((vkx - qx) ** 2 + (vky - qy) ** 2)
+    dp = vk2 - ((vkx + qx) ** 2 + (vky + qy) ** 2)
+    d = np.where(tminus, dm, np.where(tplus, dp, 0.0))
+    x = math.pi * lam * float(depth_A) * d / 2.0
+    return np.sinc(x / math.pi)  # numpy's sinc is sin(pi u)/(pi u)
+
+
+def reduce_depth(G, geom, ab, bf_idx, depth_A, entries=None, chunk=512):
+    """reduce() with the depth-spread weights w * sinc(pi lambda t D / 2)."""
+    n = G.shape[1]
+    h = n // 2 + 1
+    if entries is None:
+        entries = np.arange(n * h, dtype=np.int64)
+    entries = np.asarray(entries, dtype=np.int64)
+    qx_col, qy_row = q_coords(geom)
+    Gf = G.reshape(G.shape[0], n * h)
+    O = np.zeros(len(entries), dtype=np.complex128)
+    N = np.zeros(len(entries), dtype=np.int64)
+    for s in range(0, len(entries), chunk):
+        e = entries[s:s + chunk]
+        qx = qx_col[e % h]
+        qy = qy_row[e // h]
+        tm, tp = trotters(geom, ab, bf_idx, qx, qy)
+        w = weights(geom, ab, bf_idx, qx, qy, tm, tp) * depth_factor(geom, ab, bf_idx, qx, qy, tm, tp, depth_A)
+        g = Gf[:, e].T
+        O[s:s + chunk] = (g * w).sum(axis=1)
+        N[s:s + chunk] = (tm | tp).sum(axis=1)
+    return O, N
+
+
+# ----------------------------------------------------------------------------
 # compact G storage: herm16 (snorm16 codes + float32 block scales) and the
 # band-compacted copy
 # ----------------------------------------------------------------------------
