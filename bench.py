@@ -578,6 +578,20 @@ def run_ours(args, ws, rank, local, pg):
     # the timed region)
     score_sweep = {} if args.no_sweep else sweep(None, bytes_score)
 
+    # the depth-spread fit: the same 8 sets, each with a 136 A defocus spread
+    # (the fit kernel's depth on the pages), one pass over the band
+    score_depth = None
+    if not args.no_sweep:
+        depths = [136.0] * B
+        t_dep = timed(lambda: ssb.score_batch_depth(G, geom, bfd, sets, depths, band_d, O=Ob, N=Nb, score=sc,
+                                                    ws=ws_s, stream=stream))
+        score_depth = {"ms": t_dep, "depth_A": 136.0, "sets": B, "terms": terms,
+                       "terms_per_s": terms / (t_dep * 1e-3),
+                       "xu_frac": 2.0 * terms / (t_dep * 1e-3) / xu_peak,
+                       "note": "per active term one sincos plus one sine and one reciprocal for the spread factor; "
+                               "xu_frac counts the sincos only",
+                       "depth0_ms": score_ms}
+
     # compact G storage (measured after the timed region, not part of the
     # step): the band-compacted complex64 copy, and herm16 with one scale per
     # q row or per BF pixel -- the packing pass, the reconstruction from it and
@@ -666,6 +680,7 @@ def run_ours(args, ws, rank, local, pg):
                    "max_count": d.get("max_count")},
         "stage_rooflines": stage_rooflines,
         "score_sweep": score_sweep,
+        "score_depth": score_depth,
         "compact": compact,
         "roofline": {"bound": "hbm", "kernel": "ssb_build_G = ssb_gather + ssb_plane512<8> on two internal streams (one C-ABI call, timed on the caller's stream)", "achieved": achieved,
                      "peak": hbm, "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,

@@ -37,7 +37,7 @@ EXPORTED = ("ssb_bf_indices", "ssb_band_indices", "ssb_workspace_bytes", "ssb_bu
             "ssb_reconstruct_noalloc", "ssb_build_G_host", "ssb_build_G_host_bytes",
             "ssb_compact_G16", "ssb_compact_band", "ssb_reconstruct_g", "ssb_score_batch_g",
             "ssb_phase_moments", "ssb_reconstruct_sums", "ssb_phase_from_sums", "ssb_peak_sincos",
-            "ssb_peak_fma")
+            "ssb_peak_fma", "ssb_score_batch_depth")
 
 G_C64, G_SN16 = 0, 1
 
@@ -124,6 +124,8 @@ def load(path: str | None = None):
     lib.ssb_phase_moments.argtypes = [S_p, G_p, c_vp, c_int, A_p, c_vp, c_vp, c_vp, c_size, c_vp]
     lib.ssb_reconstruct_sums.argtypes = [c_vp, G_p, c_vp, c_int, A_p, c_vp, c_vp, c_vp, c_vp, c_size, c_vp]
     lib.ssb_phase_from_sums.argtypes = [c_vp, c_vp, c_vp, c_int, G_p, c_vp, c_vp, c_size, c_vp]
+    lib.ssb_score_batch_depth.argtypes = [S_p, G_p, c_vp, c_int, A_p, ctypes.POINTER(c_d), c_int, c_vp, c_int,
+                                          c_vp, c_vp, c_vp, c_vp, c_size, c_vp]
     lib.ssb_peak_sincos.argtypes = [c_vp, c_int, c_int, c_vp]
     lib.ssb_peak_fma.argtypes = [c_vp, c_int, c_int, c_vp]
     lib.ssb_last_error.restype = ctypes.c_char_p
@@ -131,7 +133,7 @@ def load(path: str | None = None):
     for fn in ("ssb_bf_indices", "ssb_band_indices", "ssb_build_G", "ssb_build_G_host", "ssb_reconstruct",
                "ssb_score_batch", "ssb_reconstruct_noalloc", "ssb_compact_G16", "ssb_compact_band",
                "ssb_reconstruct_g", "ssb_score_batch_g", "ssb_phase_moments", "ssb_reconstruct_sums",
-               "ssb_phase_from_sums", "ssb_peak_sincos", "ssb_peak_fma"):
+               "ssb_phase_from_sums", "ssb_peak_sincos", "ssb_peak_fma", "ssb_score_batch_depth"):
         getattr(lib, fn).restype = c_int
     _lib = lib
     return lib
@@ -499,6 +501,40 @@ def score_batch_g(store, geom, bf_idx_dev, sets, band_dev, O=None, N=None, score
     _check("ssb_score_batch_g", lib.ssb_score_batch_g(ctypes.byref(sc), ctypes.byref(g), _ptr(bf_idx_dev), n_bf,
                                                       arr, B, _ptr(band_dev), nq, _ptr(O), _ptr(N), _ptr(score),
                                                       ws.ptr(), ws.nbytes, _stream(stream)))
+    return O, N, score
+
+
+def score_batch_depth(store, geom, bf_idx_dev, sets, depth_A, band_dev, O=None, N=None, score=None, ws=None,
+                      stream=None):
+    """score_batch_g() with a defocus spread per set (depth_A: B thicknesses in
+    Angstrom, each >= 0): every trotter term is weighted by the depth-0 weight
+    times sinc(pi lambda t D / 2).  `store` may be a GStore or a complex64
+    half-plane tensor."""
+    import torch
+    lib = load()
+    if not isinstance(store, GStore):
+        store = GStore(store)
+    g = to_geometry(geom)
+    B = len(sets)
+    if len(depth_A) != B:
+        raise ValueError("depth_A needs one value per set")
+    arr = (Aberr * max(B, 1))(*[to_aberr(s) for s in sets])
+    dep = (ctypes.c_double * max(B, 1))(*[float(t) for t in depth_A])
+    n_bf = int(bf_idx_dev.numel())
+    nq = int(band_dev.numel())
+    dev = store.G.device
+    O = torch.empty((B, nq), dtype=torch.complex64, device=dev) if O is None else O
+    N = torch.empty((B, nq), dtype=torch.int32, device=dev) if N is None else N
+    score = torch.empty((B,), dtype=torch.float64, device=dev) if score is None else score
+    if ws is None:
+        need = workspace_bytes(g, n_bf, OP_SCORE, B, nq)
+        if need == 0:
+            raise SSBError("ssb_workspace_bytes", SSB_INVALID_ARG, f"invalid sizes (B={B}, nq={nq})")
+        ws = Workspace(need, dev)
+    sc = store.c()
+    _check("ssb_score_batch_depth", lib.ssb_score_batch_depth(
+        ctypes.byref(sc), ctypes.byref(g), _ptr(bf_idx_dev), n_bf, arr, dep, B, _ptr(band_dev), nq, _ptr(O),
+        _ptr(N), _ptr(score), ws.ptr(), ws.nbytes, _stream(stream)))
     return O, N, score
 
 

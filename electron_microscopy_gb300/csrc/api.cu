@@ -220,7 +220,7 @@ static int gview_of(const ssb_gstore* s, const ssb_geometry* g, int nq, GView* v
 
 static int run_reduction(const GView& gv, const ssb_geometry* g, const int32_t* bf_idx, int n_bf,
                          const SetBatch& sb, const int32_t* qlist, int nq, float2* O, int32_t* N,
-                         void* ws, const WsLayout& Lw, int want_dc, cudaStream_t st) {
+                         void* ws, const WsLayout& Lw, int want_dc, cudaStream_t st, int depth = 0) {
     cudaError_t e;
     float4* ktab = at<float4>(ws, Lw.ktab);
     float* chik = at<float>(ws, Lw.chik);
@@ -239,6 +239,7 @@ static int run_reduction(const GView& gv, const ssb_geometry* g, const int32_t* 
     P.ktab = ktab;
     P.chik = chik;
     P.shared_tilt = 1;
+    P.depth = depth;
     for (int s = 1; s < sb.B; ++s)
         if (sb.s[s].tx != sb.s[0].tx || sb.s[s].ty != sb.s[0].ty) P.shared_tilt = 0;
     P.Opart = at<float2>(ws, Lw.Opart);
@@ -551,7 +552,8 @@ int ssb_phase_from_sums(const void* O_dev, const int32_t* N_dev, const double* g
 
 static int score_impl(const ssb_gstore* store, const ssb_geometry* geom, const int32_t* bf_idx_dev, int n_bf,
                       const ssb_aberr* sets, int B, const int32_t* band_dev, int nq, void* O_dev,
-                      int32_t* N_dev, double* score_dev, void* ws, size_t ws_bytes, void* stream) {
+                      int32_t* N_dev, double* score_dev, void* ws, size_t ws_bytes, void* stream,
+                      const double* depth_A = nullptr) {
     int rc;
     if ((rc = check_geom(geom)) != SSB_OK) return rc;
     GView gv{};
@@ -565,6 +567,10 @@ static int score_impl(const ssb_gstore* store, const ssb_geometry* geom, const i
         return fail(SSB_INVALID_ARG, "nq=%d out of range", nq);
     for (int s = 0; s < B; ++s)
         if ((rc = check_set(&sets[s])) != SSB_OK) return rc;
+    if (depth_A)
+        for (int s = 0; s < B; ++s)
+            if (!std::isfinite(depth_A[s]) || depth_A[s] < 0.0)
+                return fail(SSB_INVALID_ARG, "depth_A[%d] must be finite and >= 0", s);
     const WsLayout Lw = layout(geom, n_bf, SSB_OP_SCORE, B, nq);
     if ((rc = check_ws(ws, ws_bytes, Lw.total)) != SSB_OK) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -572,8 +578,13 @@ static int score_impl(const ssb_gstore* store, const ssb_geometry* geom, const i
     sb.B = B;
     sb.r2 = aperture_r2(geom);
     for (int s = 0; s < B; ++s) sb.s[s] = set_params(geom, &sets[s]);
+    int depth = 0;
+    for (int s = 0; depth_A && s < B; ++s) {
+        sb.depth_a[s] = (float)(M_PI * geom->wavelength_A * depth_A[s] / 2.0);
+        if (depth_A[s] > 0.0) depth = 1;
+    }
     if ((rc = run_reduction(gv, geom, bf_idx_dev, n_bf, sb, band_dev, nq, static_cast<float2*>(O_dev), N_dev,
-                            ws, Lw, 0, st)) != SSB_OK)
+                            ws, Lw, 0, st, depth)) != SSB_OK)
         return rc;
     cudaError_t e;
     if ((e = launch_score(static_cast<const float2*>(O_dev), N_dev, B, nq, score_dev, st)) != cudaSuccess)
@@ -608,6 +619,14 @@ int ssb_score_batch_g(const ssb_gstore* G, const ssb_geometry* geom, const int32
                       int32_t* N_dev, double* score_dev, void* ws, size_t ws_bytes, void* stream) {
     return score_impl(G, geom, bf_idx_dev, n_bf, sets, B, band_dev, nq, O_dev, N_dev, score_dev, ws, ws_bytes,
                       stream);
+}
+
+int ssb_score_batch_depth(const ssb_gstore* G, const ssb_geometry* geom, const int32_t* bf_idx_dev, int n_bf,
+                          const ssb_aberr* sets, const double* depth_A, int B, const int32_t* band_dev, int nq,
+                          void* O_dev, int32_t* N_dev, double* score_dev, void* ws, size_t ws_bytes, void* stream) {
+    if (!depth_A) return fail(SSB_INVALID_ARG, "depth_A must not be NULL");
+    return score_impl(G, geom, bf_idx_dev, n_bf, sets, B, band_dev, nq, O_dev, N_dev, score_dev, ws, ws_bytes,
+                      stream, depth_A);
 }
 
 int ssb_phase_moments(const ssb_gstore* store, const ssb_geometry* geom, const int32_t* bf_idx_dev, int n_bf,

@@ -261,6 +261,7 @@ struct SetParams {
 
 struct SetBatch {
     SetParams s[SSB_MAX_SETS];
+    float depth_a[SSB_MAX_SETS];  // pi lambda t / 2 per set (depth-spread fit; 0: none)
     float r2;       // float32((alpha/lambda)^2)
     int B;
 };
@@ -322,15 +323,36 @@ __device__ __forceinline__ float chi_horner(float h0, float4 a, float x) {
     return __fmaf_rn(__fmaf_rn(__fmaf_rn(__fmaf_rn(h0, x, a.x), x, a.y), x, a.z), x, a.w);
 }
 
-// Aperture test, float32 contract: dx = px - tx; dy = py - ty;
-// d2 = dx*dx + dy*dy (each rounded separately); inside iff d2 <= r2.
+// Squared distance from the tilt centre, float32 contract: dx = px - tx;
+// dy = py - ty; d2 = dx*dx + dy*dy, each operation rounded separately.
+__device__ __forceinline__ float d2_f32(float px, float py, float tx, float ty) {
+    const float dx = __fsub_rn(px, tx), dy = __fsub_rn(py, ty);
+    return __fadd_rn(__fmul_rn(dx, dx), __fmul_rn(dy, dy));
+}
+
+// Aperture test, float32 contract: inside iff d2_f32(...) <= r2; also
+// returns dx, dy (and d2 in the second form).
 __device__ __forceinline__ bool aperture_f32(float px, float py, float tx, float ty, float r2,
-                                             float* dxo, float* dyo) {
+                                             float* dxo, float* dyo, float* d2o) {
     const float dx = __fsub_rn(px, tx), dy = __fsub_rn(py, ty);
     const float d2 = __fadd_rn(__fmul_rn(dx, dx), __fmul_rn(dy, dy));
     *dxo = dx;
     *dyo = dy;
+    *d2o = d2;
     return d2 <= r2;
+}
+__device__ __forceinline__ bool aperture_f32(float px, float py, float tx, float ty, float r2,
+                                             float* dxo, float* dyo) {
+    float d2;
+    return aperture_f32(px, py, tx, ty, r2, dxo, dyo, &d2);
+}
+
+// sinc(a D) = sin(a D) / (a D), 1 near 0, from the fast sine: the depth-spread
+// factor of a trotter term (a = pi lambda t / 2, D a difference of squared
+// distances in 1/A^2)
+__device__ __forceinline__ float depth_sinc(float a, float D) {
+    const float x = __fmul_rn(a, D);
+    return fabsf(x) < 1e-4f ? 1.0f : __fdividef(__sinf(x), x);
 }
 
 // w(q,k) G(q,k) added to acc: d = chi(k) - chi(k -/+ q) in turns, reduced to
@@ -408,6 +430,7 @@ struct RedLaunch {
     float2* Opart;          // [nsplit][B][nq]
     int* Npart;             // [nsplit][B][nq]
     int shared_tilt;        // every set has the same float32 tilt centre
+    int depth;              // weights include the depth-spread factor (SetBatch::depth_a)
 };
 
 // dcpart (may be null): per-256-pixel-block sums of Re G(0,k) in float64
@@ -416,6 +439,7 @@ cudaError_t launch_prep(const int32_t* bf_idx, int n_bf, int det_x, double cy, d
                         const SetBatch& sb, float4* ktab, float* chik, const GView& g,
                         double* dcpart, cudaStream_t st);
 cudaError_t launch_reduce(const RedLaunch& L, const SetBatch& sb, cudaStream_t st);
+cudaError_t launch_reduce_depth(const RedLaunch& L, const SetBatch& sb, cudaStream_t st);  // reduce_depth.cu
 cudaError_t launch_finalize(const float2* Opart, const int* Npart, int nsplit, int B, int nq,
                             float2* O, int32_t* N, cudaStream_t st);
 cudaError_t launch_phase(const float2* O, const int32_t* N, const double* dcpart, int nsplit,

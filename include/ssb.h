@@ -328,6 +328,32 @@ int ssb_score_batch_g(const ssb_gstore* G, const ssb_geometry* geom,
                       void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Batched scoring with a depth (defocus) spread per set: ssb_score_batch_g
+ * with each trotter term's weight multiplied by the real factor
+ * sinc(pi lambda t_s D / 2), sinc(x) = sin(x)/x, where t_s = depth_A[s] is set
+ * s's spread (Angstrom; the defocus runs uniformly over C10 +/- t_s/2) and D =
+ * |v_k|^2 - |v_{k-q}|^2 on T-, |v_k|^2 - |v_{k+q}|^2 on T+ (v = k - k_t, the
+ * squared distances of the float32 aperture tests).  That factor is the mean
+ * of exp(i pi lambda z D) over the spread, so the weight is the depth-0 weight
+ * times the transfer's own attenuation.  N counts trotter pixels and the score
+ * is sum |O|^2 / sum N as in ssb_score_batch.  t_s = 0 gives ssb_score_batch_g
+ * bit for bit; set s does not depend on B (bit for bit).  Source:
+ * "Tilt-corrected SSB on CUDA", sections "Changes" (the fit kernel at depth
+ * 136 A: two sincos and two sin per term) and "Results" (the depth spread is a
+ * fitted parameter); "Where the 9 s of regularized preparation goes", list
+ * item 2 (chi, sinc and phase factor of a transfer term).  The pages do not
+ * write the depth model out; this is the plainest reading.
+ * depth_A: host array of B values, each finite and >= 0.  Errors as
+ * ssb_score_batch_g, plus SSB_INVALID_ARG for a NULL, negative or non-finite
+ * depth.
+ */
+int ssb_score_batch_depth(const ssb_gstore* G, const ssb_geometry* geom,
+                          const int32_t* bf_idx_dev, int n_bf, const ssb_aberr* sets,
+                          const double* depth_A, int B, const int32_t* band_dev, int nq,
+                          void* O_dev, int32_t* N_dev, double* score_dev,
+                          void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Per-BF phase moments at one aberration set (set: host pointer): for every BF
  * pixel k, the corrected plane S_k(q) = G(q,k) w(q,k) on the trotter pixels
  * of k (0 elsewhere, and at DC and on the Nyquist row and column), its image
