@@ -16,7 +16,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libssb.so")
 
-SOURCES = ("api.cu", "build.cu", "plane.cu", "reduce.cu", "reduce_depth.cu", "compact.cu", "moments.cu", "noalloc.cu", "peaks.cu")
+SOURCES = ("api.cu", "build.cu", "plane.cu", "reduce.cu", "reduce_depth.cu", "recon_tma.cu", "compact.cu", "moments.cu", "noalloc.cu", "peaks.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-I", INCLUDE,
          "-Xcompiler", "-fPIC,-ffp-contract=off,-O2"]

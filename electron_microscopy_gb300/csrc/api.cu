@@ -112,22 +112,34 @@ static float aperture_r2(const ssb_geometry* g) {
 // ---------------------------------------------------------------------------
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Number of k-splits of the reduction: enough CTAs for ~2 waves on a
-// 152-SM part at 8 resident CTAs each; depends only on (nq, n_bf) so that the
-// summation order is the same for every B.
+// Number of k-splits of the reduction.  The grid is (nq / 256) x splits CTAs
+// of equal length; a wave is 152 SMs x 4 resident CTAs, and a partly filled
+// last wave takes about as long as a full one, so the count is the smallest
+// one (from two waves up) whose CTAs fill at least 97 % of their waves, else
+// the best filling one; at most 64 splits and about 16 k per split.  Depends
+// only on (nq, n_bf), so that the summation order is the same for every B.
 static int red_splits(int nq, int n_bf) {
-    const int bx = (nq + 255) / 256;
-    int s = (2 * 152 * 8 + bx - 1) / bx;
-    if (s < 1) s = 1;
-    if (s > 64) s = 64;
-    const int max_s = (n_bf + 15) / 16;  // at least 16 k per split
-    if (s > max_s) s = max_s;
-    if (s < 1) s = 1;
-    return s;
+    const long bx = (nq + 255) / 256, wave = 152 * 4;
+    int max_s = (n_bf + 15) / 16;
+    if (max_s > 64) max_s = 64;
+    if (max_s < 1) max_s = 1;
+    int lo = (int)((2 * wave + bx - 1) / bx);
+    if (lo > max_s) lo = max_s;
+    if (lo < 1) lo = 1;
+    auto fill = [&](int s) {
+        const long ctas = bx * s, waves = (ctas + wave - 1) / wave;
+        return (double)ctas / (double)(waves * wave);
+    };
+    int best = lo;
+    for (int s = lo; s <= max_s; ++s) {
+        if (fill(s) >= 0.97) return s;
+        if (fill(s) > fill(best)) best = s;
+    }
+    return best;
 }
 
 struct WsLayout {
-    size_t tw, xbuf, ktab, chik, Opart, Npart, dcpart, Y, total;
+    size_t tw, xbuf, ktab, chik, kxcol, status, Opart, Npart, dcpart, Y, total;
 };
 
 static WsLayout layout(const ssb_geometry* g, int n_bf, int op, int B, int nq) {
@@ -171,6 +183,10 @@ static WsLayout layout(const ssb_geometry* g, int n_bf, int op, int B, int nq) {
     off += align256((size_t)n_bf * sizeof(float4));
     L.chik = off;
     off += align256((size_t)n_bf * kChiStride * sizeof(float));
+    L.kxcol = off;
+    off += align256((size_t)g->det_x * sizeof(float));
+    L.status = off;
+    off += align256(sizeof(int));
     L.Opart = off;
     off += align256((size_t)ns * B * nq * sizeof(float2));
     L.Npart = off;
@@ -224,8 +240,10 @@ static int run_reduction(const GView& gv, const ssb_geometry* g, const int32_t* 
     cudaError_t e;
     float4* ktab = at<float4>(ws, Lw.ktab);
     float* chik = at<float>(ws, Lw.chik);
+    float* kxcol = at<float>(ws, Lw.kxcol);
     if ((e = launch_prep(bf_idx, n_bf, g->det_x, g->det_center_y, g->det_center_x, g->det_pitch_invA, sb,
-                         ktab, chik, gv, want_dc ? at<double>(ws, Lw.dcpart) : nullptr, st)) != cudaSuccess)
+                         ktab, chik, kxcol, at<int>(ws, Lw.status), gv, want_dc ? at<double>(ws, Lw.dcpart) : nullptr,
+                         st)) != cudaSuccess)
         return cuda_fail(e, "prep");
     RedLaunch P{};
     P.g = gv;
@@ -238,6 +256,11 @@ static int run_reduction(const GView& gv, const ssb_geometry* g, const int32_t* 
     P.qlist = qlist;
     P.ktab = ktab;
     P.chik = chik;
+    P.kxcol = kxcol;
+    P.status = at<int>(ws, Lw.status);
+    P.ncol = g->det_x;
+    P.inv_dk = (float)(1.0 / g->det_pitch_invA);
+    P.ccol = (float)g->det_center_x;
     P.shared_tilt = 1;
     P.depth = depth;
     for (int s = 1; s < sb.B; ++s)
@@ -245,7 +268,7 @@ static int run_reduction(const GView& gv, const ssb_geometry* g, const int32_t* 
     P.Opart = at<float2>(ws, Lw.Opart);
     P.Npart = at<int>(ws, Lw.Npart);
     if ((e = launch_reduce(P, sb, st)) != cudaSuccess) return cuda_fail(e, "reduce");
-    if ((e = launch_finalize(P.Opart, P.Npart, P.nsplit, sb.B, nq, O, N, st)) != cudaSuccess)
+    if ((e = launch_finalize(P.Opart, P.Npart, P.nsplit, sb.B, nq, P.status, O, N, st)) != cudaSuccess)
         return cuda_fail(e, "finalize");
     return SSB_OK;
 }
@@ -654,7 +677,7 @@ int ssb_phase_moments(const ssb_gstore* store, const ssb_geometry* geom, const i
     cudaError_t e;
     if ((e = launch_twiddles(tw, geom->n, st)) != cudaSuccess) return cuda_fail(e, "twiddles");
     if ((e = launch_prep(bf_idx_dev, n_bf, geom->det_x, geom->det_center_y, geom->det_center_x, geom->det_pitch_invA,
-                         sb, ktab, at<float>(ws, Lw.chik), gv, nullptr, st)) != cudaSuccess)
+                         sb, ktab, at<float>(ws, Lw.chik), nullptr, nullptr, gv, nullptr, st)) != cudaSuccess)
         return cuda_fail(e, "prep");
     if ((e = launch_moments(gv, geom->n, n_bf, ktab, sb, 1.0 / ((double)geom->n * geom->scan_step_A), tw,
                             at<void>(ws, Lw.Y), at<void>(ws, Lw.Opart), mean_dev, var_dev, st)) != cudaSuccess)

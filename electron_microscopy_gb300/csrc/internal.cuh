@@ -397,6 +397,9 @@ cudaError_t launch_build512(const uint16_t* frames, int det_pix, const int32_t* 
 // bits of the sets as float bits, chi_0(k) in turns); chi_s(k) of every set
 // in chik[k * kChiStride + s]
 constexpr int kChiStride = 8;
+// ktab[k].z bits: bit s the aperture test of set s at k; kRowStart marks a
+// pixel whose detector row differs from the previous list entry's
+constexpr uint32_t kRowStart = 0x80000000u;
 
 // a stored G as the reductions read it: complex64 entries, or herm16 words
 // (two int16 codes, real in the low half) with float32 scales
@@ -427,8 +430,12 @@ struct RedLaunch {
     const int32_t* qlist;   // null: identity over the half plane
     float4* ktab;           // [n_bf]
     float* chik;            // [n_bf][kChiStride]
+    const float* kxcol;     // [ncol]: float32 k_x of each detector column, as in ktab
+    int ncol;
+    float inv_dk, ccol;     // 1 / detector pitch, column of k_x = 0 (starting points only)
     float2* Opart;          // [nsplit][B][nq]
     int* Npart;             // [nsplit][B][nq]
+    int* status;            // nonzero after a kernel wait ran out (zeroed by the prep kernel)
     int shared_tilt;        // every set has the same float32 tilt centre
     int depth;              // weights include the depth-spread factor (SetBatch::depth_a)
 };
@@ -436,12 +443,17 @@ struct RedLaunch {
 // dcpart (may be null): per-256-pixel-block sums of Re G(0,k) in float64
 // (G must then be a half plane: entry 0 is q = 0)
 cudaError_t launch_prep(const int32_t* bf_idx, int n_bf, int det_x, double cy, double cx, double dk,
-                        const SetBatch& sb, float4* ktab, float* chik, const GView& g,
+                        const SetBatch& sb, float4* ktab, float* chik, float* kxcol, int* status, const GView& g,
                         double* dcpart, cudaStream_t st);
 cudaError_t launch_reduce(const RedLaunch& L, const SetBatch& sb, cudaStream_t st);
+// the single-set pass over the whole half plane with TMA-streamed G rows
+// (recon_tma.cu), where the layout allows it (complex64 half plane, 16-byte
+// aligned rows)
+bool recon_tma_applies(const RedLaunch& P, const SetBatch& sb);
+cudaError_t launch_recon_tma(const RedLaunch& P, const SetBatch& sb, cudaStream_t st);
 cudaError_t launch_reduce_depth(const RedLaunch& L, const SetBatch& sb, cudaStream_t st);  // reduce_depth.cu
 cudaError_t launch_finalize(const float2* Opart, const int* Npart, int nsplit, int B, int nq,
-                            float2* O, int32_t* N, cudaStream_t st);
+                            const int* status, float2* O, int32_t* N, cudaStream_t st);
 cudaError_t launch_phase(const float2* O, const int32_t* N, const double* dcpart, int nsplit,
                          int n_bf, int n, float2* Y, const float2* tw, float* phase,
                          cudaStream_t st);

@@ -12,7 +12,8 @@
 //   exactly as ssb_reconstruct checks them (same status codes); then calls
 //   whose scratch need (ssb_workspace_bytes(..., SSB_OP_RECON, ...)) exceeds
 //   the array are rejected with SSB_UNSUPPORTED before anything is launched.
-//   16 MiB covers every n <= 512 (the full 512^2 workload needs ~9.3 MiB) but
+//   16 MiB covers every n <= 512 (the full 512^2 workload needs ~12 MiB, and
+//   13.3 MiB with a whole 192 x 192 detector bright) but
 //   not n = 1024.
 // * Host code cannot use the array's name as a device address, so every call
 //   asks the runtime for the address on the current device with

@@ -29,8 +29,14 @@ namespace ssb {
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256)
 ssb_prep(const int32_t* __restrict__ bf_idx, int n_bf, int det_x, double cy, double cx, double dk, SetBatch sb,
-         float4* __restrict__ ktab, float* __restrict__ chik, GView g, double* __restrict__ dcpart) {
+         float4* __restrict__ ktab, float* __restrict__ chik, float* __restrict__ kxcol, int* __restrict__ status,
+         GView g, double* __restrict__ dcpart) {
     const int k = blockIdx.x * blockDim.x + threadIdx.x;
+    if (status && k == 0) *status = 0;
+    // k_x of every detector column, by the same expression as a BF pixel's
+    if (kxcol && blockIdx.x == 0)
+        for (int j = threadIdx.x; j < det_x; j += blockDim.x)
+            kxcol[j] = __double2float_rn(__dmul_rn(__dsub_rn((double)j, cx), dk));
     if (dcpart) {
         // sum_k Re G(0, k) for the image offset a: per-block partial in
         // float64, added in a fixed order by the image kernel (entry 0 of a
@@ -70,19 +76,24 @@ ssb_prep(const int32_t* __restrict__ bf_idx, int n_bf, int det_x, double cy, dou
         if (s == 0) chi0 = c;
         chik[(size_t)k * kChiStride + s] = c;
     }
+    // the first pixel of a detector row in list order (a different row
+    // from the previous list entry) carries kRowStart
+    if (k == 0 || bf_idx[k - 1] / det_x != i) bits |= kRowStart;
     ktab[k] = make_float4(kx, ky, __uint_as_float(bits), chi0);
 }
 
 cudaError_t launch_prep(const int32_t* bf_idx, int n_bf, int det_x, double cy, double cx, double dk,
-                        const SetBatch& sb, float4* ktab, float* chik, const GView& g,
-                        double* dcpart, cudaStream_t st) {
-    ssb_prep<<<(n_bf + 255) / 256, 256, 0, st>>>(bf_idx, n_bf, det_x, cy, cx, dk, sb, ktab, chik, g, dcpart);
+                        const SetBatch& sb, float4* ktab, float* chik, float* kxcol, int* status,
+                        const GView& g, double* dcpart, cudaStream_t st) {
+    ssb_prep<<<(n_bf + 255) / 256, 256, 0, st>>>(bf_idx, n_bf, det_x, cy, cx, dk, sb, ktab, chik, kxcol, status, g,
+                                                 dcpart);
     count_launch();
     return cudaGetLastError();
 }
 
 cudaError_t launch_reduce(const RedLaunch& P, const SetBatch& sb, cudaStream_t st) {
     if (P.depth) return launch_reduce_depth(P, sb, st);
+    if (recon_tma_applies(P, sb)) return launch_recon_tma(P, sb, st);
     return launch_reduce_t<false>(P, sb, st);
 }
 
@@ -90,11 +101,16 @@ cudaError_t launch_reduce(const RedLaunch& P, const SetBatch& sb, cudaStream_t s
 // partial sums -> O, N (fixed order over splits)
 // ---------------------------------------------------------------------------
 __global__ void ssb_finalize(const float2* __restrict__ Opart, const int* __restrict__ Npart,
-                                int nsplit, int B, int nq, float2* __restrict__ O,
-                                int32_t* __restrict__ N) {
+                                int nsplit, int B, int nq, const int* __restrict__ status,
+                                float2* __restrict__ O, int32_t* __restrict__ N) {
     const size_t t = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     const size_t total = (size_t)B * nq;
     if (t >= total) return;
+    if (status && *status) {  // a reduction wait ran out: no valid sums
+        O[t] = make_float2(__int_as_float(0x7fc00000), __int_as_float(0x7fc00000));
+        N[t] = -1;
+        return;
+    }
     float2 a = Opart[t];
     int c = Npart[t];
     for (int sp = 1; sp < nsplit; ++sp) {
@@ -108,9 +124,9 @@ __global__ void ssb_finalize(const float2* __restrict__ Opart, const int* __rest
 }
 
 cudaError_t launch_finalize(const float2* Opart, const int* Npart, int nsplit, int B, int nq,
-                            float2* O, int32_t* N, cudaStream_t st) {
+                            const int* status, float2* O, int32_t* N, cudaStream_t st) {
     const size_t total = (size_t)B * nq;
-    ssb_finalize<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(Opart, Npart, nsplit, B, nq, O, N);
+    ssb_finalize<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(Opart, Npart, nsplit, B, nq, status, O, N);
     count_launch();
     return cudaGetLastError();
 }

@@ -37,6 +37,61 @@ constexpr size_t red_smem_bytes() {
 template <int MAXB, bool SHARED>
 __host__ __device__ constexpr int red_min_blocks() { return (MAXB == 1 || SHARED) ? 4 : 2; }
 
+// The aperture test at k -/+ q on one detector row.  Along a row (k_y
+// fixed) the float32 test d2 = (dx*dx + dy*dy) <= r2, dx = (k_x -/+ q_x) - t_x,
+// holds on a contiguous run of columns: dx is a rounded monotone function of
+// k_x, dx*dx is rounded monotone on either side of dx = 0, and the sum is
+// rounded monotone in it.  row_run returns the k_x of the run's first and
+// last column (+inf, -inf: no column), so that for a pixel of the row the
+// test equals lo <= k_x <= hi exactly.  The run is located by testing
+// columns: the smallest d2 on the grid is at one of the columns next to the
+// centre k_x = t_x +/- q_x, so the run is empty unless one of those passes;
+// its ends are walked from estimates given by the circle's half-width.
+struct RowRun {
+    float lo, hi;
+};
+__device__ __forceinline__ RowRun row_run(const float* __restrict__ kxcol, int ncol, float inv_dk, float ccol,
+                                          float ky, float qx, float qy, bool minus, float tx, float ty, float r2) {
+    const RowRun none{__int_as_float(0x7f800000), __int_as_float(0xff800000)};
+    const float dy = __fsub_rn(minus ? __fsub_rn(ky, qy) : __fadd_rn(ky, qy), ty);
+    const float yy = __fmul_rn(dy, dy);
+    if (!(yy <= r2)) return none;  // d2 >= yy at every column
+    auto pass = [&](int j) {
+        const float kx = __ldg(kxcol + j);
+        const float dx = __fsub_rn(minus ? __fsub_rn(kx, qx) : __fadd_rn(kx, qx), tx);
+        return __fadd_rn(__fmul_rn(dx, dx), yy) <= r2;
+    };
+    // fractional column of the centre, and the circle's half-width in columns
+    const float cc = fmaf(minus ? (tx + qx) : (tx - qx), inv_dk, ccol);
+    const float hw = sqrtf(r2 - yy) * inv_dk;
+    const float top = (float)(ncol - 1);
+    const int j0 = (int)rintf(fminf(fmaxf(cc, 0.0f), top));
+    int js;
+    if (pass(j0))
+        js = j0;
+    else if (j0 > 0 && pass(j0 - 1))
+        js = j0 - 1;
+    else if (j0 < ncol - 1 && pass(j0 + 1))
+        js = j0 + 1;
+    else
+        return none;
+    // first column: from the estimate, walk to the run's edge (the walks stay
+    // within [0, js] and [js, ncol - 1]: js passes)
+    int a = min((int)ceilf(fminf(fmaxf(cc - hw, 0.0f), top)), js);
+    if (pass(a)) {
+        while (a > 0 && pass(a - 1)) --a;
+    } else {
+        while (!pass(a)) ++a;
+    }
+    int b = max((int)floorf(fminf(fmaxf(cc + hw, 0.0f), top)), js);
+    if (pass(b)) {
+        while (b < ncol - 1 && pass(b + 1)) ++b;
+    } else {
+        while (!pass(b)) --b;
+    }
+    return RowRun{__ldg(kxcol + a), __ldg(kxcol + b)};
+}
+
 // DEPTH: each set's terms are also weighted by the defocus-spread factor
 // sinc(a_s D), a_s = pi lambda t_s / 2, D = |v_k|^2 - |v_{k-/+q}|^2 (the
 // squared distances the aperture tests already form, so the factor is a
@@ -78,7 +133,9 @@ ssb_reduce(RedLaunch P, SetBatch sb) {
     // more: the warp's shared-memory table, indexed by the lane's row slot.
     extern __shared__ float4 rowtab[];
     float4 row_m = make_float4(0.f, 0.f, 0.f, 0.f), row_p = row_m;
-    float cur_ky = __int_as_float(0x7fc00000);  // NaN: no row yet
+    // one set: the columns of the current row where the aperture test at
+    // k - q (run_m) and at k + q (run_p) holds
+    RowRun run_m{0.0f, 0.0f}, run_p{0.0f, 0.0f};
     const int lane = threadIdx.x & 31;
     float4* wtab = rowtab + (size_t)(threadIdx.x >> 5) * kRowSlots * 2 * row_tab_stride<MAXB>();
     int slot = 0, nslots = 1;
@@ -142,35 +199,49 @@ ssb_reduce(RedLaunch P, SetBatch sb) {
             return gs;
         }
     };
-    auto step = [&](const GIn& g, float4 kd, const float* chk, auto tab) {
-        if (decltype(tab)::value && kd.y != cur_ky) {  // uniform: every lane walks the same k
-            new_row(kd.y);
-            cur_ky = kd.y;
+    // the row state at a pixel that starts a detector row, or the split's
+    // first pixel (uniform: every lane walks the same k): one set, the
+    // aperture runs and the row polynomials; more sets, the row table
+    constexpr bool RUNS = SHARED && MAXB == 1;
+    auto row_enter = [&](float ky) {
+        if constexpr (RUNS) {
+            run_m = row_run(P.kxcol, P.ncol, P.inv_dk, P.ccol, ky, qx, qy, true, sb.s[0].tx, sb.s[0].ty, sb.r2);
+            run_p = row_run(P.kxcol, P.ncol, P.inv_dk, P.ccol, ky, qx, qy, false, sb.s[0].tx, sb.s[0].ty, sb.r2);
         }
+        new_row(ky);
+    };
+    auto step = [&](const GIn& g, float4 kd, const float* chk, auto tab) {
         const uint32_t am = __float_as_uint(kd.z);
-        const float mx = __fsub_rn(kd.x, qx), my = __fsub_rn(kd.y, qy);
-        const float px = __fadd_rn(kd.x, qx), py = __fadd_rn(kd.y, qy);
-        if constexpr (SHARED && MAXB == 1) {
-            // one set: no branch, so the unrolled k steps can overlap; the
-            // result is committed only on a single-overlap pixel
-            float mvx, mvy, pvx, pvy, d2m, d2p;
-            const bool m = aperture_f32(mx, my, sb.s[0].tx, sb.s[0].ty, sb.r2, &mvx, &mvy, &d2m);
-            const bool p = aperture_f32(px, py, sb.s[0].tx, sb.s[0].ty, sb.r2, &pvx, &pvy, &d2p);
+        if constexpr (RUNS) {
+            // one set: the aperture tests are comparisons with the row's
+            // runs; the result is committed only on a single-overlap pixel
+            const bool m = kd.x >= run_m.lo && kd.x <= run_m.hi;
+            const bool p = kd.x >= run_p.lo && kd.x <= run_p.hi;
             const bool act = (am & 1u) && (m != p);
             // warp-uniform skip: lanes of a warp hold neighbouring q, so whole
             // warps often have no trotter pixel at this k
             if (__any_sync(0xffffffffu, act)) {
                 // inactive lanes add an exact zero: gs = 0 * G, and every
-                // later term is finite
+                // later term is finite.  The side's offset: k_x - (-q_x) is
+                // the same float as k_x + q_x
+                const float qsx = m ? qx : -qx;
                 const float sg = act ? (m ? 1.0f : -1.0f) : 0.0f;
                 const float2 gv = gval(g);
-                const float d2k = DEPTH ? d2_f32(kd.x, kd.y, sb.s[0].tx, sb.s[0].ty) : 0.0f;
-                accumulate(acc[0],
-                           depth_w(0, make_float2(__fmul_rn(sg, gv.x), __fmul_rn(sg, gv.y)), d2k, m ? d2m : d2p),
-                           kd.w, chi_v(tab, 0, m, m ? mvx : pvx, 0.f), m ? kTwoPi : -kTwoPi);
+                const float x = __fsub_rn(__fsub_rn(kd.x, qsx), sb.s[0].tx);
+                float d2k = 0.0f, d2o = 0.0f;
+                if constexpr (DEPTH) {
+                    d2k = d2_f32(kd.x, kd.y, sb.s[0].tx, sb.s[0].ty);
+                    d2o = d2_f32(__fsub_rn(kd.x, qsx), __fsub_rn(kd.y, m ? qy : -qy), sb.s[0].tx, sb.s[0].ty);
+                }
+                accumulate(acc[0], depth_w(0, make_float2(__fmul_rn(sg, gv.x), __fmul_rn(sg, gv.y)), d2k, d2o),
+                           kd.w, chi_v(tab, 0, m, x, 0.f), m ? kTwoPi : -kTwoPi);
                 cnt[0] += act ? 1 : 0;
             }
-        } else if constexpr (SHARED) {
+            return;
+        }
+        const float mx = __fsub_rn(kd.x, qx), my = __fsub_rn(kd.y, qy);
+        const float px = __fadd_rn(kd.x, qx), py = __fadd_rn(kd.y, qy);
+        if constexpr (SHARED) {
             // one tilt for all sets: the aperture tests are common, only the
             // row polynomial, the phase and the accumulation run per set
             if (am & 1u) {
@@ -222,37 +293,59 @@ ssb_reduce(RedLaunch P, SetBatch sb) {
     // as short broadcasts and the registers go to G loads in flight
     __shared__ float4 s_ktab[kKChunk];
     __shared__ float4 s_chik[MAXB > 1 ? kKChunk * kChiStride / 4 : 1];
+    // A chunk is walked in row segments: the row state is rebuilt once at a
+    // segment's start (a pixel marked kRowStart, or the split's first pixel),
+    // and within a segment the k steps run in batches of U with no row check.
     auto walk = [&](auto tab, int kc0, int kcn) {
         constexpr int U = red_unroll<MAXB>();
+        constexpr bool ROWS = decltype(tab)::value;
         [[maybe_unused]] const float2* gk = gp + (size_t)kc0 * gstride;
         [[maybe_unused]] const uint32_t* wk = gw + (size_t)kc0 * gstride;
         [[maybe_unused]] const float* sk = gsc + kc0;
         int i = 0;
 #pragma unroll 1
-        for (; i + U <= kcn; i += U) {
-            GIn g[U];
-            if constexpr (FMT == kGC64) {
+        while (i < kcn) {
+            int e = kcn;  // end of this segment
+            if constexpr (ROWS) {
+                if (i > 0 || kc0 == kb || (__float_as_uint(s_ktab[0].z) & kRowStart)) row_enter(s_ktab[i].y);
+                // the next row start within the chunk (uniform search)
+#pragma unroll 1
+                for (int j0 = i + 1; j0 < kcn; j0 += 32) {
+                    const int j = j0 + lane;
+                    const unsigned bal =
+                        __ballot_sync(0xffffffffu, j < kcn && (__float_as_uint(s_ktab[j].z) & kRowStart));
+                    if (bal) {
+                        e = j0 + __ffs(bal) - 1;
+                        break;
+                    }
+                }
+            }
+#pragma unroll 1
+            for (; i + U <= e; i += U) {
+                GIn g[U];
+                if constexpr (FMT == kGC64) {
+#pragma unroll
+                    for (int u = 0; u < U; ++u)
+                        g[u] = valid ? __ldcs(gk + (size_t)(i + u) * gstride) : make_float2(0.f, 0.f);
+                } else {
+#pragma unroll
+                    for (int u = 0; u < U; ++u) g[u].x = valid ? __ldcs(wk + (size_t)(i + u) * gstride) : 0u;
+#pragma unroll
+                    for (int u = 0; u < U; ++u) g[u].y = __float_as_uint(__ldg(sk + i + u));
+                }
 #pragma unroll
                 for (int u = 0; u < U; ++u)
-                    g[u] = valid ? __ldcs(gk + (size_t)(i + u) * gstride) : make_float2(0.f, 0.f);
-            } else {
-#pragma unroll
-                for (int u = 0; u < U; ++u) g[u].x = valid ? __ldcs(wk + (size_t)(i + u) * gstride) : 0u;
-#pragma unroll
-                for (int u = 0; u < U; ++u) g[u].y = __float_as_uint(__ldg(sk + i + u));
+                    step(g[u], s_ktab[i + u], reinterpret_cast<const float*>(s_chik) + (i + u) * kChiStride, tab);
             }
-#pragma unroll
-            for (int u = 0; u < U; ++u)
-                step(g[u], s_ktab[i + u], reinterpret_cast<const float*>(s_chik) + (i + u) * kChiStride, tab);
-        }
 #pragma unroll 1
-        for (; i < kcn; ++i) {
-            GIn g;
-            if constexpr (FMT == kGC64)
-                g = valid ? __ldcs(gk + (size_t)i * gstride) : make_float2(0.f, 0.f);
-            else
-                g = make_uint2(valid ? __ldcs(wk + (size_t)i * gstride) : 0u, __float_as_uint(__ldg(sk + i)));
-            step(g, s_ktab[i], reinterpret_cast<const float*>(s_chik) + i * kChiStride, tab);
+            for (; i < e; ++i) {
+                GIn g;
+                if constexpr (FMT == kGC64)
+                    g = valid ? __ldcs(gk + (size_t)i * gstride) : make_float2(0.f, 0.f);
+                else
+                    g = make_uint2(valid ? __ldcs(wk + (size_t)i * gstride) : 0u, __float_as_uint(__ldg(sk + i)));
+                step(g, s_ktab[i], reinterpret_cast<const float*>(s_chik) + i * kChiStride, tab);
+            }
         }
     };
 #pragma unroll 1
