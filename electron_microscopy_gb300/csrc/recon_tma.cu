@@ -2,11 +2,14 @@
 // half plane (the reconstruction's pass), with the G rows streamed into
 // shared memory by bulk asynchronous copies (TMA) instead of per-thread loads.
 //
-// Terms, order and float32 arithmetic are those of ssb_reduce<1, shared
-// tilt, complex64> (reduce.cu, reduce_kernel.cuh): a block owns 256
-// consecutive half-plane entries q, grid.y splits the bright-field list, and
-// each block walks its split's pixels k in list order.  What differs is how
-// G(q, k) reaches the threads:
+// The terms, their order and the trotter classification are those of
+// ssb_reduce<1, shared tilt, complex64> (reduce.cu, reduce_kernel.cuh): a
+// block owns 256 consecutive half-plane entries q, grid.y splits the
+// bright-field list, and each block walks its split's pixels k in list
+// order.  Two things differ.  The float32 evaluation of a term is leaner:
+// chi(k -/+ q) comes from a per-row quartic in k_x, and the T+ sign is
+// folded into the phase (see step below).  And G(q, k) reaches the threads
+// through shared memory:
 //
 //  * the split's pixels are taken in groups of kTmaPix; a group's G row
 //    segments (256 entries, 2 KB each) and its k-table entries are copied
@@ -90,6 +93,25 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
+// coefficients (a3, a2, a1, a0) of P(y - s) for the quartic
+// P(x) = h0 x^4 + a3 x^3 + a2 x^2 + a1 x + a0 (Taylor shift by repeated
+// synthetic division; the leading coefficient stays h0)
+__device__ __forceinline__ float4 shift_quartic(float h0, float4 a, float s) {
+    const float ns = -s;
+    float b1 = a.x, b2 = a.y, b3 = a.z, b4 = a.w;
+    b1 = __fmaf_rn(ns, h0, b1);
+    b2 = __fmaf_rn(ns, b1, b2);
+    b3 = __fmaf_rn(ns, b2, b3);
+    b4 = __fmaf_rn(ns, b3, b4);
+    b1 = __fmaf_rn(ns, h0, b1);
+    b2 = __fmaf_rn(ns, b1, b2);
+    b3 = __fmaf_rn(ns, b2, b3);
+    b1 = __fmaf_rn(ns, h0, b1);
+    b2 = __fmaf_rn(ns, b1, b2);
+    b1 = __fmaf_rn(ns, h0, b1);
+    return make_float4(b1, b2, b3, b4);
+}
+
 __global__ void __launch_bounds__(kTmaThreads, 4) ssb_recon_tma(RedLaunch P, SetBatch sb) {
     extern __shared__ __align__(128) unsigned char tma_smem[];
     TmaRing& R = *reinterpret_cast<TmaRing*>(tma_smem);
@@ -140,30 +162,40 @@ __global__ void __launch_bounds__(kTmaThreads, 4) ssb_recon_tma(RedLaunch P, Set
     float4 row_m = make_float4(0.f, 0.f, 0.f, 0.f), row_p = row_m;
     RowRun run_m{0.0f, 0.0f}, run_p{0.0f, 0.0f};
     // the row state at a pixel that starts a detector row (or the split's
-    // first pixel): the aperture runs at k -/+ q and chi(k -/+ q) as quartics
-    // in v_x along the row
+    // first pixel): the aperture runs at k -/+ q, and chi(k -/+ q) along the
+    // row as a quartic in k_x itself (the quartic in v_x = k_x - s, shifted
+    // by s = t_x +/- q_x), so that a step evaluates it at k_x directly
     auto row_enter = [&](float ky) {
         run_m = row_run(P.kxcol, P.ncol, P.inv_dk, P.ccol, ky, qx, qy, true, sb.s[0].tx, sb.s[0].ty, sb.r2);
         run_p = row_run(P.kxcol, P.ncol, P.inv_dk, P.ccol, ky, qx, qy, false, sb.s[0].tx, sb.s[0].ty, sb.r2);
-        row_m = chi_row(sb.s[0].h, __fsub_rn(__fsub_rn(ky, qy), sb.s[0].ty));
-        row_p = chi_row(sb.s[0].h, __fsub_rn(__fadd_rn(ky, qy), sb.s[0].ty));
+        row_m = shift_quartic(sb.s[0].h[0], chi_row(sb.s[0].h, __fsub_rn(__fsub_rn(ky, qy), sb.s[0].ty)),
+                              __fadd_rn(qx, sb.s[0].tx));
+        row_p = shift_quartic(sb.s[0].h[0], chi_row(sb.s[0].h, __fsub_rn(__fadd_rn(ky, qy), sb.s[0].ty)),
+                              __fsub_rn(sb.s[0].tx, qx));
     };
-    // one pixel: the aperture tests are comparisons with the row's runs; a
-    // single-overlap pixel adds +/-G w; the warp skips pixels no lane uses
-    // (inactive lanes add an exact zero)
+    // one pixel: the aperture tests are comparisons with the row's runs.  A
+    // single-overlap pixel adds G exp(-2 pi i r), r the phase in turns
+    // reduced to [-1/2, 1/2]: on T-, of d = chi(k) - chi(k - q); on T+, of
+    // -d - 1/2 (d = chi(k) - chi(k + q)), since -exp(2 pi i d) equals
+    // exp(-2 pi i (-d - 1/2)).  The warp skips pixels no lane uses; inside,
+    // only active lanes accumulate.
     auto step = [&](const float2* gsrc, float4 kd) {
         const uint32_t am = __float_as_uint(kd.z);
         const bool m = kd.x >= run_m.lo && kd.x <= run_m.hi;
         const bool p = kd.x >= run_p.lo && kd.x <= run_p.hi;
         const bool act = (am & 1u) && (m != p);
         if (__any_sync(0xffffffffu, act)) {
-            const float qsx = m ? qx : -qx;  // k_x - (-q_x) is the same float as k_x + q_x
-            const float sg = act ? (m ? 1.0f : -1.0f) : 0.0f;
             const float2 gv = *gsrc;
-            const float x = __fsub_rn(__fsub_rn(kd.x, qsx), sb.s[0].tx);
-            accumulate(acc, make_float2(__fmul_rn(sg, gv.x), __fmul_rn(sg, gv.y)), kd.w,
-                       chi_horner(sb.s[0].h[0], m ? row_m : row_p, x), m ? kTwoPi : -kTwoPi);
-            cnt += act ? 1 : 0;
+            const float d = __fsub_rn(kd.w, chi_horner(sb.s[0].h[0], m ? row_m : row_p, kd.x));
+            const float ds = m ? d : __fsub_rn(-0.5f, d);
+            const float r = __fsub_rn(ds, rintf(ds));
+            float sn, cs;
+            __sincosf(__fmul_rn(kTwoPi, r), &sn, &cs);  // |argument| <= pi
+            if (act) {
+                acc.x = __fmaf_rn(gv.y, sn, __fmaf_rn(gv.x, cs, acc.x));
+                acc.y = __fmaf_rn(-gv.x, sn, __fmaf_rn(gv.y, cs, acc.y));
+                cnt += 1;
+            }
         }
     };
 
