@@ -17,6 +17,10 @@ Workloads (scan n x n at 0.373 A, 300 kV, 30 mrad):
   the band 0.2 <= |q| <= 0.9 1/A.
 * ``large`` as ``full`` on a 1024^2 scan.
 * ``mid``   512^2 scan with the 64^2 detector of ``small`` (profiling case).
+* ``middet`` 256^2 scan, 128^2 detector at the ``full`` sampling (~9.3k BF
+  pixels; profiling case for the reductions).
+* ``midlarge`` 1024^2 scan, 32^2 detector (~250 BF pixels; profiling case for
+  the two-pass n = 1024 build).
 
 The sources for these numbers are the MoS2 / crystal scans of the quantem.gpu
 SSB reports (2026-10-24 regularized preparation, "Setup"; 2026-10-20 tilt
@@ -121,6 +125,13 @@ WORKLOADS = {
     # profiling case: the full scan size with the small detector (2.1 GB of
     # frames, ~1k BF pixels) so that many-pass counter captures stay small
     "mid": Workload("mid", 5, 512, 64, 30.0 / 18.0, "u16", 3.0, "hex"),
+    # profiling case for the reductions: the full workload's detector sampling
+    # and aperture (~9.3k BF pixels, rows of ~86 pixels; the 109-pixel BF disc
+    # fits a 128^2 detector) on a 256^2 scan: 2.1 GB of frames, 2.5 GB of G
+    "middet": Workload("middet", 6, 256, 128, 0.551, "u16", 3.0, "hex"),
+    # profiling case for the two-pass n = 1024 build: the large scan with a
+    # 32^2 detector (BF radius ~9 px, ~250 BF pixels): 2.1 GB of frames, 1 GB of G
+    "midlarge": Workload("midlarge", 7, 1024, 32, 30.0 / 9.0, "u16", 3.0, "hex"),
 }
 
 
