@@ -164,13 +164,21 @@ int ssb_build_G(const void* frames, int dtype, const ssb_geometry* geom,
  * Only bright-field pixels carry G ("Historical WebGPU G(q,k) memory
  * experiment", sections "Implementation" and "Gotchas recorded"), so only
  * their bounding box on the detector crosses the host link: rows r0..r1 and
- * columns c0..c1 are the extremes of bf_idx_host, and one pitched copy on
- * `stream` moves that box of every frame into the workspace (a 2D copy of
- * whole rows when the box spans the detector's width, else a 3D copy).  The
- * build then runs as ssb_build_G on the GPU machine; G_dev is bit-identical to what
- * ssb_build_G gives on device frames.
+ * columns c0..c1 are the extremes of bf_idx_host (c0 rounded down to an
+ * even column unless the box spans the detector's width), and one pitched
+ * copy moves that box of every frame into the workspace (a 2D copy of whole
+ * rows when the box spans the detector's width, else a 3D copy).  The copy
+ * runs on a library-internal stream of the device (created on the first
+ * call, kept for the process) that carries the copies of every
+ * ssb_build_G_host call in call order: it waits on an event recorded on
+ * `stream`, and `stream` waits on its completion, so ordering against the
+ * caller's stream is as for a copy on `stream`, while the copy of the next
+ * call (from another stream) can start as soon as this one ends.  The build
+ * then runs on `stream` as ssb_build_G on the box; G_dev is bit-identical to
+ * what ssb_build_G gives on device frames.
  * frames_host: (n, n, det_y, det_x) uint16 or float32, contiguous; it must
- * stay valid and unmodified until the copy has completed on `stream`.
+ * stay valid and unmodified until the copy has completed (any later work on
+ * `stream` completing implies it).
  * bf_idx_host, bf_idx_dev: the same n_bf detector indices, host and device
  * copies.  The workspace must hold ssb_build_G_host_bytes() bytes.
  * Errors as ssb_build_G, plus SSB_INVALID_ARG for a host index outside the
