@@ -643,6 +643,9 @@ static int score_impl(const ssb_gstore* store, const ssb_geometry* geom, const i
     sb.B = B;
     sb.r2 = aperture_r2(geom);
     for (int s = 0; s < B; ++s) sb.s[s] = set_params(geom, &sets[s]);
+    // the batched kernels compute a compile-time number of sets (2, 4 or 8);
+    // the slots past B hold copies of set 0, whose sums are never written
+    for (int s = B; s < SSB_MAX_SETS; ++s) sb.s[s] = sb.s[0];
     int depth = 0;
     for (int s = 0; depth_A && s < B; ++s) {
         sb.depth_a[s] = (float)(M_PI * geom->wavelength_A * depth_A[s] / 2.0);

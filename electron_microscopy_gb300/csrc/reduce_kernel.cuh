@@ -163,7 +163,7 @@ ssb_reduce(RedLaunch P, SetBatch sb) {
                 float4* e = wtab + (size_t)lane * row_tab_stride<MAXB>();
 #pragma unroll
                 for (int s = 0; s < MAXB; ++s)
-                    if (s < sb.B) e[s] = chi_row(sb.s[s].h, __fsub_rn(kq, sb.s[s].ty));
+                    e[s] = chi_row(sb.s[s].h, __fsub_rn(kq, sb.s[s].ty));
             }
             __syncwarp();
         }
@@ -265,15 +265,18 @@ ssb_reduce(RedLaunch P, SetBatch sb) {
                         if (4 * v4 + 2 < MAXB) ck[4 * v4 + 2] = c4.z;
                         if (4 * v4 + 3 < MAXB) ck[4 * v4 + 3] = c4.w;
                     }
+                    // every set's term runs unconditionally (sets past B
+                    // are copies of set 0, their sums never written), so the
+                    // sets' dependent chains can interleave
 #pragma unroll
                     for (int s = 0; s < MAXB; ++s)
-                        if (s < sb.B) accumulate(acc[s], depth_w(s, gs, d2k, d2o), ck[s], chi_v(tab, s, m, x, y), tw);
+                        accumulate(acc[s], depth_w(s, gs, d2k, d2o), ck[s], chi_v(tab, s, m, x, y), tw);
                 }
             }
         } else {
 #pragma unroll
             for (int s = 0; s < MAXB; ++s) {
-                if (s < sb.B && ((am >> s) & 1u)) {
+                if ((am >> s) & 1u) {  // no aperture bits past B
                     float mvx, mvy, pvx, pvy, d2m, d2p;
                     const bool m = aperture_f32(mx, my, sb.s[s].tx, sb.s[s].ty, sb.r2, &mvx, &mvy, &d2m);
                     const bool p = aperture_f32(px, py, sb.s[s].tx, sb.s[s].ty, sb.r2, &pvx, &pvy, &d2p);
