@@ -177,25 +177,24 @@ __global__ void __launch_bounds__(kTmaThreads, 4) ssb_recon_tma(RedLaunch P, Set
     // single-overlap pixel adds G exp(-2 pi i r), r the phase in turns
     // reduced to [-1/2, 1/2]: on T-, of d = chi(k) - chi(k - q); on T+, of
     // -d - 1/2 (d = chi(k) - chi(k + q)), since -exp(2 pi i d) equals
-    // exp(-2 pi i (-d - 1/2)).  The warp skips pixels no lane uses; inside,
-    // only active lanes accumulate.
+    // exp(-2 pi i (-d - 1/2)).  Every lane evaluates every pixel's term and
+    // only active lanes accumulate: with no branch between them, the pixels'
+    // dependent chains can interleave.
     auto step = [&](const float2* gsrc, float4 kd) {
         const uint32_t am = __float_as_uint(kd.z);
         const bool m = kd.x >= run_m.lo && kd.x <= run_m.hi;
         const bool p = kd.x >= run_p.lo && kd.x <= run_p.hi;
         const bool act = (am & 1u) && (m != p);
-        if (__any_sync(0xffffffffu, act)) {
-            const float2 gv = *gsrc;
-            const float d = __fsub_rn(kd.w, chi_horner(sb.s[0].h[0], m ? row_m : row_p, kd.x));
-            const float ds = m ? d : __fsub_rn(-0.5f, d);
-            const float r = __fsub_rn(ds, rintf(ds));
-            float sn, cs;
-            __sincosf(__fmul_rn(kTwoPi, r), &sn, &cs);  // |argument| <= pi
-            if (act) {
-                acc.x = __fmaf_rn(gv.y, sn, __fmaf_rn(gv.x, cs, acc.x));
-                acc.y = __fmaf_rn(-gv.x, sn, __fmaf_rn(gv.y, cs, acc.y));
-                cnt += 1;
-            }
+        const float2 gv = *gsrc;
+        const float d = __fsub_rn(kd.w, chi_horner(sb.s[0].h[0], m ? row_m : row_p, kd.x));
+        const float ds = m ? d : __fsub_rn(-0.5f, d);
+        const float r = __fsub_rn(ds, rintf(ds));
+        float sn, cs;
+        __sincosf(__fmul_rn(kTwoPi, r), &sn, &cs);  // |argument| <= pi
+        if (act) {
+            acc.x = __fmaf_rn(gv.y, sn, __fmaf_rn(gv.x, cs, acc.x));
+            acc.y = __fmaf_rn(-gv.x, sn, __fmaf_rn(gv.y, cs, acc.y));
+            cnt += 1;
         }
     };
 
