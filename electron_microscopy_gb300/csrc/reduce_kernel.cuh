@@ -13,7 +13,7 @@ namespace ssb {
 // fused reduction
 // ---------------------------------------------------------------------------
 constexpr int kRedThreads = 256;
-constexpr int kKChunk = 64;  // k pixels whose tables a block stages at a time
+constexpr int kKChunk = 256;  // k pixels whose tables a block stages at a time
 // k steps whose G loads are issued together: the single-set pass streams G
 // and is bound by load latency, so it keeps more loads in flight
 template <int MAXB>
