@@ -274,19 +274,32 @@ ssb_reduce(RedLaunch P, SetBatch sb) {
                 }
             }
         } else {
+            // sets with their own tilts: every set's two aperture tests first;
+            // then, if any lane has a single-overlap pixel in any set, every
+            // set's term, an inactive one with zero weight, so that the sets'
+            // dependent chains can interleave (sets past B have no aperture
+            // bits and never contribute)
+            uint32_t mbits = 0u, pbits = 0u;
 #pragma unroll
             for (int s = 0; s < MAXB; ++s) {
-                if ((am >> s) & 1u) {  // no aperture bits past B
-                    float mvx, mvy, pvx, pvy, d2m, d2p;
-                    const bool m = aperture_f32(mx, my, sb.s[s].tx, sb.s[s].ty, sb.r2, &mvx, &mvy, &d2m);
-                    const bool p = aperture_f32(px, py, sb.s[s].tx, sb.s[s].ty, sb.r2, &pvx, &pvy, &d2p);
-                    if (m != p) {
-                        const float cq = chi_v(tab, s, m, m ? mvx : pvx, m ? mvy : pvy);
-                        const float d2k = DEPTH ? d2_f32(kd.x, kd.y, sb.s[s].tx, sb.s[s].ty) : 0.0f;
-                        accumulate(acc[s], depth_w(s, side_sign(gval(g), m), d2k, m ? d2m : d2p), chk[s], cq,
-                                   m ? kTwoPi : -kTwoPi);
-                        cnt[s] += 1;
-                    }
+                float vx, vy;
+                mbits |= (aperture_f32(mx, my, sb.s[s].tx, sb.s[s].ty, sb.r2, &vx, &vy) ? 1u : 0u) << s;
+                pbits |= (aperture_f32(px, py, sb.s[s].tx, sb.s[s].ty, sb.r2, &vx, &vy) ? 1u : 0u) << s;
+            }
+            const uint32_t actb = am & (mbits ^ pbits);
+            if (__any_sync(0xffffffffu, actb != 0u)) {
+                const float2 gv = gval(g);
+#pragma unroll
+                for (int s = 0; s < MAXB; ++s) {
+                    const bool m = (mbits >> s) & 1u, act = (actb >> s) & 1u;
+                    // the side's (v_x, v_y) as the aperture test formed them
+                    const float x = __fsub_rn(m ? mx : px, sb.s[s].tx), y = __fsub_rn(m ? my : py, sb.s[s].ty);
+                    const float2 gs = act ? side_sign(gv, m) : make_float2(0.f, 0.f);
+                    const float d2k = DEPTH ? d2_f32(kd.x, kd.y, sb.s[s].tx, sb.s[s].ty) : 0.0f;
+                    const float d2o = DEPTH ? __fadd_rn(__fmul_rn(x, x), __fmul_rn(y, y)) : 0.0f;
+                    accumulate(acc[s], depth_w(s, gs, d2k, d2o), chk[s], chi_v(tab, s, m, x, y),
+                               m ? kTwoPi : -kTwoPi);
+                    cnt[s] += act ? 1 : 0;
                 }
             }
         }
