@@ -651,6 +651,9 @@ static int score_impl(const ssb_gstore* store, const ssb_geometry* geom, const i
         sb.depth_a[s] = (float)(M_PI * geom->wavelength_A * depth_A[s] / 2.0);
         if (depth_A[s] > 0.0) depth = 1;
     }
+    sb.depth_shared = 1;
+    for (int s = 1; s < B; ++s)
+        if (sb.depth_a[s] != sb.depth_a[0]) sb.depth_shared = 0;
     if ((rc = run_reduction(gv, geom, bf_idx_dev, n_bf, sb, band_dev, nq, static_cast<float2*>(O_dev), N_dev,
                             ws, Lw, 0, st, depth)) != SSB_OK)
         return rc;

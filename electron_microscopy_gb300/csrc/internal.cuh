@@ -262,6 +262,7 @@ struct SetParams {
 struct SetBatch {
     SetParams s[SSB_MAX_SETS];
     float depth_a[SSB_MAX_SETS];  // pi lambda t / 2 per set (depth-spread fit; 0: none)
+    int depth_shared;             // every set has the same depth_a
     float r2;       // float32((alpha/lambda)^2)
     int B;
 };

@@ -267,10 +267,19 @@ ssb_reduce(RedLaunch P, SetBatch sb) {
                     }
                     // every set's term runs unconditionally (sets past B
                     // are copies of set 0, their sums never written), so the
-                    // sets' dependent chains can interleave
+                    // sets' dependent chains can interleave.  With one tilt
+                    // the spread factor depends on the set only through its
+                    // depth: when all sets share it, it is taken once
+                    if (DEPTH && sb.depth_shared) {
+                        const float2 g1 = depth_w(0, gs, d2k, d2o);
 #pragma unroll
-                    for (int s = 0; s < MAXB; ++s)
-                        accumulate(acc[s], depth_w(s, gs, d2k, d2o), ck[s], chi_v(tab, s, m, x, y), tw);
+                        for (int s = 0; s < MAXB; ++s)
+                            accumulate(acc[s], g1, ck[s], chi_v(tab, s, m, x, y), tw);
+                    } else {
+#pragma unroll
+                        for (int s = 0; s < MAXB; ++s)
+                            accumulate(acc[s], depth_w(s, gs, d2k, d2o), ck[s], chi_v(tab, s, m, x, y), tw);
+                    }
                 }
             }
         } else {

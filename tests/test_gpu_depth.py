@@ -43,6 +43,25 @@ def small(ssb, small_dataset):
     return d, bf, G, band, O.build_G(fr, bf)
 
 
+@pytest.mark.parametrize("B", [2, 8])
+def test_shared_depth_matches_oracle_and_single_sets(ssb, small, B):
+    """Every set at the same spread (136 A, the pages' fit depth): the factor is
+    taken once per (q, k) for all sets.  Each set matches the oracle and equals
+    the same set scored alone, bit for bit."""
+    d, bf, G, band, Gor = small
+    g = d["geom"]
+    bfd, bd = torch.from_numpy(bf).cuda(), torch.from_numpy(band).cuda()
+    sets = C.perturbed_sets(d["ab"], B, seed=90 + B)
+    Ob, Nb, sc = ssb.score_batch_depth(G, g, bfd, sets, [136.0] * B, bd)
+    torch.cuda.synchronize()
+    for s, ab in enumerate(sets):
+        Oref, Nref = O.reduce_depth(Gor, g, ab, bf, 136.0, entries=band)
+        assert np.array_equal(Nb[s].cpu().numpy(), Nref), s
+        assert rel(Ob[s].cpu().numpy(), Oref) < TOL, s
+        O1, N1, s1 = ssb.score_batch_depth(G, g, bfd, [ab], [136.0], bd)
+        assert torch.equal(O1[0], Ob[s]) and torch.equal(N1[0], Nb[s]) and torch.equal(s1[0], sc[s]), s
+
+
 @pytest.mark.parametrize("B", [1, 3, 8])
 def test_depth_scores_match_oracle(ssb, small, B):
     d, bf, G, band, Gor = small
