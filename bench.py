@@ -616,8 +616,9 @@ def run_ours(args, ws, rank, local, pg):
         score_depth = {"ms": t_dep, "depth_A": 136.0, "sets": B, "terms": terms,
                        "terms_per_s": terms / (t_dep * 1e-3),
                        "xu_frac": 2.0 * terms / (t_dep * 1e-3) / xu_peak,
-                       "note": "per active term one sincos plus one sine and one reciprocal for the spread factor; "
-                               "xu_frac counts the sincos only",
+                       "note": "all sets at one spread with one tilt: the spread factor (a sine and a reciprocal) "
+                               "once per active (q, k) pair, one sincos per active term; xu_frac counts the sincos "
+                               "only",
                        "depth0_ms": score_ms}
 
     # compact G storage (measured after the timed region, not part of the
