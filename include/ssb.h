@@ -201,6 +201,12 @@ size_t ssb_build_G_host_bytes(const ssb_geometry* geom, int dtype, const int32_t
  * (float32 [n][n], row = scan_y).  Source: "Historical WebGPU G(q,k) memory
  * experiment", section "Object-redraw fast path"; "Tilt-corrected SSB on
  * CUDA", sections "Changes" and "Open".
+ * When G_dev is 16-byte aligned (and n is even) the pass streams G's rows
+ * through shared memory with bulk asynchronous copies whose barrier waits are
+ * bounded in time; a wait that runs out (possible only after a fault
+ * elsewhere on the device) cannot be reported by the asynchronous call, so it
+ * leaves NaN in O_dev and phase_dev and -1 in N_dev instead.  Any other G_dev
+ * alignment runs the same sums with per-thread loads.
  */
 int ssb_reconstruct(const void* G_dev, const ssb_geometry* geom,
                     const int32_t* bf_idx_dev, int n_bf, const ssb_aberr* set,
