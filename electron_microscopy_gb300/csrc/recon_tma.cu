@@ -269,12 +269,9 @@ bool recon_tma_applies(const RedLaunch& P, const SetBatch& sb) {
 
 cudaError_t launch_recon_tma(const RedLaunch& P, const SetBatch& sb, cudaStream_t st) {
     const size_t smem = sizeof(TmaRing);
-    static bool opted = false;  // idempotent attribute; a racing second set is harmless
-    if (!opted) {
-        const cudaError_t e = cudaFuncSetAttribute(ssb_recon_tma, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        opted = true;
-    }
+    // set on every call: the attribute belongs to the current device's context
+    const cudaError_t e = cudaFuncSetAttribute(ssb_recon_tma, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
     dim3 grid((P.nq + kTmaThreads - 1) / kTmaThreads, P.nsplit);
     ssb_recon_tma<<<grid, kTmaThreads, smem, st>>>(P, sb);
     count_launch();

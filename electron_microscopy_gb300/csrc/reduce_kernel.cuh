@@ -405,14 +405,9 @@ ssb_reduce(RedLaunch P, SetBatch sb) {
 template <int MAXB, bool SHARED, int FMT, bool DEPTH>
 static void launch_reduce_bsf(const RedLaunch& P, const SetBatch& sb, dim3 grid, cudaStream_t st) {
     constexpr size_t smem = red_smem_bytes<MAXB>();
-    if (smem > 48 * 1024) {
-        static bool opted = false;  // idempotent attribute; a racing second set is harmless
-        if (!opted) {
-            cudaFuncSetAttribute(ssb_reduce<MAXB, SHARED, FMT, DEPTH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
-            opted = true;
-        }
-    }
+    if (smem > 48 * 1024)  // set on every call: the attribute belongs to the current device's context
+        cudaFuncSetAttribute(ssb_reduce<MAXB, SHARED, FMT, DEPTH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
     ssb_reduce<MAXB, SHARED, FMT, DEPTH><<<grid, kRedThreads, smem, st>>>(P, sb);
 }
 
