@@ -288,6 +288,32 @@ def test_reconstruct_is_deterministic(ssb, small_G):
         assert torch.equal(x, y)
 
 
+def test_build_G_host_on_two_streams(ssb, small_dataset):
+    """Host-input builds issued on two streams in turn, one stream reusing its
+    workspace while its previous build may still be reading it: the copies
+    queue on the library's copy stream, yet every build sees its own frames
+    (each G bit for bit the device-input build of the same frames)."""
+    d = small_dataset
+    g, ab = d["geom"], d["ab"]
+    bf = O.bf_indices(g, ab.tilt_x_rad, ab.tilt_y_rad)
+    bfd = _dev(bf)
+    f1 = d["frames"]
+    f2 = np.ascontiguousarray(f1[::-1, ::-1])  # another scan: frames in reverse scan order
+    ref = [ssb.build_G(_frames_dev(f), g, bfd) for f in (f1, f2)]
+    hosts = [torch.from_numpy(f.view(np.int16)).pin_memory() for f in (f1, f2)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    ws = [ssb.Workspace(ssb.build_G_host_bytes(g, bf, ssb.SSB_U16), bfd.device) for _ in range(2)]
+    order = [(0, 0), (1, 1), (0, 1), (1, 0), (0, 0), (1, 1)]  # (stream and workspace, frames)
+    out = []
+    for lane, fi in order:
+        G = torch.empty_like(ref[0])
+        ssb.build_G_host(hosts[fi], g, bf, bfd, G=G, ws=ws[lane], stream=streams[lane])
+        out.append((G, fi))
+    torch.cuda.synchronize()
+    for G, fi in out:
+        assert torch.equal(G, ref[fi])
+
+
 @pytest.mark.parametrize("case", ["tiny", "small", "n512", "whole"])
 def test_build_G_host_equals_device_build(ssb, case, tiny_dataset, small_dataset):
     """The host-input build copies only the bright-field bounding box of each
